@@ -1,0 +1,169 @@
+"""Block-pool allocator model: integers only, one Python statement per rule.
+
+Test infrastructure only (see ``oracle/__init__``).
+
+What the pages fix:
+* the KV state of a request is a logical sequence of fixed-size blocks drawn from
+  a shared pool as tokens arrive; a per-request block table maps logical order to
+  physical blocks ("¿Cómo gestiona Paged Attention la caché KV...?", section
+  "PagedAttention divide el estado KV en bloques de tamaño fijo"; "PagedAttention
+  e vLLM", "Approfondimento tecnico"; "Paged Attention optimiza el uso de memoria
+  en LLMs", paragraph on 16-token pages and the page table);
+* when a request ends its unshared blocks return to the shared pool at once
+  (same zimaspace page, "Los bloques liberados regresan a un conjunto compartido");
+* the runtime keeps reference counts ("La gestión de bloques tiene sus propios
+  costes"); cancellation releases references without freeing pages still in use
+  ("Servicio de modelos de lenguaje con un presupuesto de memoria" §8);
+* identical prefixes (parallel samples, beams, a shared system prompt) point at the
+  same physical pages and only the page where a request diverges is copied
+  ("PagedAttention e vLLM", "Approfondimento tecnico"; "Paged Attention optimiza...",
+  copy-on-write paragraph).
+
+Readings where the pages are silent (the same rules are the library's ABI):
+* free list order: blocks are handed out in the order of ``initial_free_list``
+  (default 0..NB-1); a freed block goes on top and is handed out next (LIFO);
+* a new or forked sequence takes the lowest unused id in [0, max_seqs);
+* copy-on-write fires on an append to a sequence whose *partially filled* last
+  block has refcount > 1: a fresh block is taken, the pair (old, new) is reported
+  for the device copy, the old block loses one reference and the table points at
+  the new block. Full shared blocks are never copied; the last holder (refcount 1)
+  writes in place;
+* slot of logical position t = table[t // B] * B + t % B;
+* every call is all-or-nothing: if the free blocks cannot cover the whole call,
+  nothing changes.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence, Tuple
+
+OK = 0
+ERR_INVALID = -1
+ERR_NO_BLOCKS = -2
+ERR_NO_SEQ = -3
+ERR_CAPACITY = -6
+
+
+class PoolModel:
+    def __init__(self, num_blocks: int, block_size: int, max_seqs: int, max_blocks_per_seq: int,
+                 initial_free_list: Optional[Sequence[int]] = None, fail_after_n_allocs: int = -1):
+        self.NB = int(num_blocks)
+        self.B = int(block_size)
+        self.max_seqs = int(max_seqs)
+        self.MB = int(max_blocks_per_seq)
+        order = list(range(self.NB)) if initial_free_list is None else [int(b) for b in initial_free_list]
+        if sorted(order) != list(range(self.NB)):
+            raise ValueError("initial_free_list must be a permutation of [0, num_blocks)")
+        # stack whose top (end of the list) is the next block handed out
+        self.free: List[int] = list(reversed(order))
+        self.refcount: List[int] = [0] * self.NB
+        self.tables: Dict[int, List[int]] = {}
+        self.lens: Dict[int, int] = {}
+        self.n_cow = 0
+        self.fail_after = int(fail_after_n_allocs)
+        self.n_allocs = 0
+
+    # -- helpers -----------------------------------------------------------------
+    def _new_id(self) -> int:
+        for s in range(self.max_seqs):
+            if s not in self.tables:
+                return s
+        return -1
+
+    def _pop(self) -> int:
+        b = self.free.pop()
+        self.refcount[b] = 1
+        return b
+
+    # -- operations --------------------------------------------------------------
+    def alloc(self, seq: int, n_tokens: int) -> Tuple[int, int, List[int], List[Tuple[int, int]]]:
+        """Append n_tokens positions to ``seq`` (-1: a new sequence).
+
+        Returns (status, seq_id, slots, cow_pairs)."""
+        if n_tokens < 0:
+            return ERR_INVALID, -1, [], []
+        if seq == -1:
+            sid = self._new_id()
+            if sid < 0:
+                return ERR_CAPACITY, -1, [], []
+            table, length = [], 0
+        else:
+            if seq not in self.tables:
+                return ERR_NO_SEQ, -1, [], []
+            sid, table, length = seq, self.tables[seq], self.lens[seq]
+        B = self.B
+        new_blocks = -(-(length + n_tokens) // B) - (-(-length // B))
+        if -(-(length + n_tokens) // B) > self.MB:
+            return ERR_CAPACITY, -1, [], []
+        cow = 1 if (n_tokens > 0 and length % B != 0 and self.refcount[table[-1]] > 1) else 0
+        if self.fail_after >= 0 and self.n_allocs >= self.fail_after:
+            return ERR_NO_BLOCKS, -1, [], []
+        if new_blocks + cow > len(self.free):
+            return ERR_NO_BLOCKS, -1, [], []
+        # commit
+        if seq == -1:
+            self.tables[sid] = table = []
+            self.lens[sid] = 0
+        slots: List[int] = []
+        pairs: List[Tuple[int, int]] = []
+        for _ in range(n_tokens):
+            if length % B == 0:
+                table.append(self._pop())
+            elif self.refcount[table[-1]] > 1:
+                old = table[-1]
+                dst = self._pop()
+                pairs.append((old, dst))
+                self.refcount[old] -= 1
+                table[-1] = dst
+            slots.append(table[length // B] * B + length % B)
+            length += 1
+        self.lens[sid] = length
+        self.n_cow += len(pairs)
+        self.n_allocs += 1
+        return OK, sid, slots, pairs
+
+    def fork(self, parent: int) -> Tuple[int, int]:
+        """New sequence sharing every block of ``parent`` (refcount + 1 each). Returns (status, child)."""
+        if parent not in self.tables:
+            return ERR_NO_SEQ, -1
+        child = self._new_id()
+        if child < 0:
+            return ERR_CAPACITY, -1
+        self.tables[child] = list(self.tables[parent])
+        self.lens[child] = self.lens[parent]
+        for b in self.tables[child]:
+            self.refcount[b] += 1
+        return OK, child
+
+    def free_seq(self, seq: int) -> int:
+        """Drop one reference to every block of ``seq`` in table order; a block at zero is freed."""
+        if seq not in self.tables:
+            return ERR_NO_SEQ
+        for b in self.tables.pop(seq):
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                self.free.append(b)
+        del self.lens[seq]
+        return OK
+
+    # -- views -------------------------------------------------------------------
+    def block_table(self, seqs: Sequence[int]) -> Tuple[List[List[int]], List[int]]:
+        rows, lens = [], []
+        for s in seqs:
+            t = self.tables[s]
+            rows.append(t + [-1] * (self.MB - len(t)))
+            lens.append(self.lens[s])
+        return rows, lens
+
+    def export_state(self) -> Tuple[List[int], List[int]]:
+        """(refcounts, free blocks from the bottom of the stack to its top)."""
+        return list(self.refcount), list(self.free)
+
+    def stats(self) -> Dict[str, int]:
+        return {
+            "num_free": len(self.free),
+            "num_used": sum(1 for r in self.refcount if r > 0),
+            "num_shared": sum(1 for r in self.refcount if r > 1),
+            "num_cow": self.n_cow,
+            "num_seqs": len(self.tables),
+            "num_tokens": sum(self.lens.values()),
+        }

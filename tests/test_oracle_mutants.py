@@ -1,0 +1,116 @@
+"""The pins must catch plausible mistakes planted in copies of the oracle (CPU only).
+
+Each mutant is a copy of an oracle routine with one mistake (dropped term, wrong sign or
+index, swapped operand). The pin checks of ``test_oracle_attention`` are run against it and
+at least one must fail. The oracle itself is never modified.
+"""
+import math
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import attention as att
+from oracle import native
+from tests.test_oracle_attention import make_problem, sdpa
+
+
+def pin_checks(fn):
+    """Run the core pins against a decode implementation; return the names of those that fail."""
+    failed = []
+    P = make_problem(7, [1, 17, 100, 53, 250], 8, 2, 64, 16, "bf16")
+    with np.errstate(all="ignore"):
+        out = fn(P["q"], P["kc"], P["vc"], P["tables"], P["lens"], P["scale"])
+        if not np.allclose(out, sdpa(P), rtol=0, atol=1e-12):
+            failed.append("sdpa")
+        P1 = make_problem(5, [1, 1], 8, 2, 64, 16, "bf16")
+        o1 = fn(P1["q"], P1["kc"], P1["vc"], P1["tables"], P1["lens"], P1["scale"])
+        if not all(np.array_equal(o1[b, j], att.to_f64(P1["logical"][b][1][0, j // 4]))
+                   for b in range(2) for j in range(8)):
+            failed.append("single_token")
+        Px = make_problem(13, [300, 7], 8, 2, 64, 16, "f32")
+        Px["q"] = (Px["q"] * 100.0).astype(np.float32)
+        ox = fn(Px["q"], Px["kc"], Px["vc"], Px["tables"], Px["lens"], Px["scale"])
+        if not (np.isfinite(ox).all() and np.allclose(ox, sdpa(Px), rtol=0, atol=1e-11)):
+            failed.append("extreme")
+    return failed
+
+
+# ---- NumPy mutants: each replaces one line of the definition ----------------------------------------
+
+def _mutant(kind):
+    def gather(cache, table, length, kv_head):
+        B = cache.shape[2]
+        if kind == "block_index":
+            rows = [cache[int(table[min(t + 1, length - 1) // B]), kv_head, t % B, :] for t in range(length)]
+        elif kind == "offset":
+            rows = [cache[int(table[t // B]), kv_head, (B - 1 - t % B), :] for t in range(length)]
+        elif kind == "drop_last":
+            rows = [cache[int(table[t // B]), kv_head, t % B, :] for t in range(max(length - 1, 1))]
+        else:
+            rows = [cache[int(table[t // B]), kv_head, t % B, :] for t in range(length)]
+        return att.to_f64(np.stack(rows))
+
+    def dense(q, K, V, scale):
+        s = (K @ q) if kind == "no_scale" else scale * (K @ q)
+        m = 0.0 if kind == "no_max" else s.max()
+        p = np.exp(s - m)
+        if kind == "no_norm":
+            return p @ V
+        if kind == "swap_kv":
+            s = scale * (V @ q)
+            p = np.exp(s - s.max())
+            return (p @ K) / p.sum()
+        return (p @ V) / p.sum()
+
+    def decode(q, k_cache, v_cache, tables, lens, scale):
+        n, Hq, D = q.shape
+        Hkv = k_cache.shape[1]
+        g = Hq // Hkv
+        qd = att.to_f64(q)
+        out = np.zeros((n, Hq, D))
+        for b in range(n):
+            L = int(lens[b])
+            for j in range(Hq):
+                h = (j % Hkv) if kind == "gqa_mod" else j // g
+                out[b, j] = dense(qd[b, j], gather(k_cache, tables[b], L, h), gather(v_cache, tables[b], L, h), scale)
+        return out
+    return decode
+
+
+def test_unmodified_oracles_pass_every_pin():
+    assert pin_checks(att.paged_decode) == []
+    assert pin_checks(native.decode) == []
+
+
+@pytest.mark.parametrize("kind", ["block_index", "offset", "drop_last", "no_scale", "no_max", "no_norm",
+                                  "swap_kv", "gqa_mod"])
+def test_numpy_mutant_is_caught(kind):
+    assert pin_checks(_mutant(kind)) != []
+
+
+# ---- C mutants: one textual edit of decode_ref.c, built into a temporary directory ------------------
+
+C_MUTANTS = {
+    "offset": ("(t % block_size)) * D;", "(block_size - 1 - t % block_size)) * D;"),
+    "gqa_mod": ("const int h = j / g;", "const int h = j % num_kv_heads;"),
+    "no_scale": ("s[t] = scale * acc;", "s[t] = acc;"),
+    "no_max": ("s[t] = exp(s[t] - m);", "s[t] = exp(s[t]);"),
+    "no_norm": ("for (int d = 0; d < D; ++d) o[d] /= l;", ""),
+    "swap_kv": ("K[(size_t)t * D + d] = load_value(k_cache", "K[(size_t)t * D + d] = load_value(v_cache"),
+    "dtype_shift": ("<< 16;", "<< 15;"),
+    "q_row": ("((size_t)b * num_q_heads + j) * D + d", "((size_t)b * num_q_heads + h) * D + d"),
+}
+
+
+@pytest.mark.parametrize("kind", sorted(C_MUTANTS))
+def test_c_mutant_is_caught(kind, tmp_path):
+    src = open(os.path.join(os.path.dirname(native.__file__), "decode_ref.c")).read()
+    old, new = C_MUTANTS[kind]
+    assert src.count(old) == 1, kind
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-o", str(so), str(mpath), "-lm"], check=True)
+    assert pin_checks(native.decode_fn_from(str(so))) != []
