@@ -1,0 +1,206 @@
+/*
+ * libpagedkv — paged KV cache and paged decode attention for NVIDIA B300 (sm_103a).
+ *
+ * C ABI. Every entry point returns a pkv_status (nothing throws across the boundary).
+ * Plain pointers and sizes only. "host" pointers are ordinary CPU memory; "device"
+ * pointers are CUDA global memory on the current device, owned by the caller. The
+ * library allocates no device memory: caches, q, outputs, tables and workspaces all
+ * belong to the caller. Device operations are enqueued on the caller's stream
+ * (a cudaStream_t passed as void*; NULL = legacy default stream) and never synchronise,
+ * except pkv_last_error.
+ *
+ * Method (sources are the pages this library implements):
+ *  - KV state of a request lives in fixed-size physical blocks of B token positions
+ *    drawn from a shared pool as tokens arrive; a per-request block table maps logical
+ *    order to physical blocks ("¿Cómo gestiona Paged Attention la caché KV cuando hay
+ *    solicitudes simultáneas de IA local?", section "PagedAttention divide el estado KV
+ *    en bloques de tamaño fijo"; "Paged Attention optimiza el uso de memoria en LLMs",
+ *    16-token pages and the page table).
+ *  - Finished requests return their unshared blocks to the pool at once (same zimaspace
+ *    page, "Los bloques liberados regresan a un conjunto compartido"); the runtime keeps
+ *    block tables and reference counts ("La gestión de bloques tiene sus propios costes").
+ *  - Identical prefixes share physical pages; only the page where a request diverges is
+ *    copied ("PagedAttention e vLLM", "Approfondimento tecnico"; the elsemanal page's
+ *    copy-on-write paragraph). Cancellation releases references without freeing pages
+ *    still in use ("Servicio de modelos de lenguaje con un presupuesto de memoria" §8).
+ *  - Decode attention is exact softmax(scale * q.K^T) V, computed blockwise with running
+ *    max/sum statistics (same page §6); GQA query heads share a KV head in contiguous
+ *    groups ("¿Cuánta memoria reservar para la caché KV?", "Emplear las cabezas KV").
+ *
+ * Cache layout (one K and one V tensor per layer, same for every layer):
+ *     cache[num_blocks][num_kv_heads][block_size][head_dim]   (dtype of the pool)
+ * Token slot s (from pkv_alloc) lives at block s / block_size, offset s % block_size.
+ * Block ids are shared by all layers: one block table serves every layer, since every
+ * layer stores every token (per-token budget 2*L*Hkv*D*bytes, the auturnal page §3).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_VERSION 1
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef struct pkv_pool pkv_pool; /* opaque; the library owns all host metadata */
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = -1,        /* bad argument (null pointer, size, alignment, dtype, unsupported shape) */
+  PKV_ERR_NO_BLOCKS = -2,      /* pool has too few free blocks for the whole call (or injected failure) */
+  PKV_ERR_NO_SEQ = -3,         /* sequence id is not live */
+  PKV_ERR_CUDA = -4,           /* a CUDA runtime call failed (launch, attribute, device query) */
+  PKV_ERR_DEVICE_BOUNDS = -5,  /* a kernel met a block id or slot outside the pool and skipped it */
+  PKV_ERR_CAPACITY = -6,       /* max_seqs or max_blocks_per_seq would be exceeded */
+  PKV_ERR_DEVICE_TIMEOUT = -7  /* a kernel gave up waiting for a copy it issued (bounded wait) */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+typedef struct {
+  int32_t num_layers;          /* layers sharing the block table (>= 1) */
+  int32_t num_kv_heads;        /* Hkv (>= 1) */
+  int32_t head_dim;            /* D; device ops support 64 and 128 */
+  int32_t block_size;          /* B tokens per block (>= 1; device ops need a multiple of 16) */
+  int32_t num_blocks;          /* NB physical blocks in the pool */
+  int32_t max_seqs;            /* sequence ids are 0 .. max_seqs-1 */
+  int32_t max_blocks_per_seq;  /* MB: row length of block tables */
+  int32_t dtype;               /* pkv_dtype of q, K and V */
+  const int32_t* initial_free_list; /* host, optional: permutation of [0, NB) giving the order in
+                                       which blocks are first handed out; NULL = 0, 1, ..., NB-1.
+                                       Copied at create time. */
+  int32_t fail_after_n_allocs; /* host fault injection: once this many pkv_alloc/pkv_append calls
+                                  have succeeded, later ones fail with PKV_ERR_NO_BLOCKS and change
+                                  nothing. -1 = off. */
+} pkv_pool_desc;
+
+typedef struct {
+  int32_t num_free;    /* blocks on the free list */
+  int32_t num_used;    /* blocks with refcount > 0 */
+  int32_t num_shared;  /* blocks with refcount > 1 */
+  int32_t num_seqs;    /* live sequences */
+  int64_t num_cow;     /* copy-on-write pairs emitted since creation */
+  int64_t num_tokens;  /* sum of live sequence lengths */
+} pkv_stats;
+
+/* ---- library info ----------------------------------------------------------------------- */
+
+PKV_API int pkv_version(void);
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* ---- pool (host) -------------------------------------------------------------------------- */
+
+/* Create a pool. desc is read and copied (host). On success *out owns the pool. Errors:
+ * PKV_ERR_INVALID for non-positive sizes, an unknown dtype or a list that is not a permutation. */
+PKV_API pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out);
+PKV_API void pkv_pool_destroy(pkv_pool* pool);
+
+/* Bytes of K plus V per token across all layers: 2 * L * Hkv * D * sizeof(dtype)
+ * ("Servicio de modelos de lenguaje con un presupuesto de memoria" §3). */
+PKV_API int64_t pkv_bytes_per_token(const pkv_pool* pool);
+/* Bytes of ONE cache tensor (K or V) of ONE layer: NB * Hkv * B * D * sizeof(dtype). */
+PKV_API int64_t pkv_layer_cache_bytes(const pkv_pool* pool);
+
+/* ---- allocator (host only, no device work, all-or-nothing) ---------------------------------- */
+
+/* Append n_tokens >= 0 positions to sequence seq (seq = -1: create a new sequence, which takes
+ * the lowest unused id). For every appended position, in order: if the sequence length is a
+ * multiple of B a free block is taken (free list order, LIFO reuse); otherwise, if the partially
+ * filled last block has refcount > 1, it is copied on write: a free block dst is taken, the pair
+ * (last, dst) is reported, the old block loses a reference and the table points at dst. The slot
+ * of position t is table[t / B] * B + t % B.
+ * Outputs (host): *seq_out; slots_out[n_tokens] (int64); cow_pairs_out[2] receives (src, dst) when
+ * *n_cow_out == 1 (at most one copy per call). slots_out may be NULL when n_tokens == 0.
+ * Check order: n_tokens < 0 -> INVALID; new id unavailable -> CAPACITY; seq not live -> NO_SEQ;
+ * ceil((len + n) / B) > max_blocks_per_seq -> CAPACITY; injected failure -> NO_BLOCKS;
+ * free blocks < blocks needed -> NO_BLOCKS. On error nothing changes. */
+PKV_API pkv_status pkv_alloc(pkv_pool* pool, int32_t seq, int32_t n_tokens, int32_t* seq_out, int64_t* slots_out,
+                     int32_t* cow_pairs_out, int32_t* n_cow_out);
+
+/* One decode step: append ONE position to each of n distinct live sequences seqs[0..n), in that
+ * order, with the pkv_alloc rules. Host outputs: slots_out[n] (int64), cow_pairs_out[2 * n] holding
+ * *n_cow_out (src, dst) pairs in emission order. All-or-nothing for the whole batch (duplicate ids:
+ * PKV_ERR_INVALID). Counts as one call for fail_after_n_allocs. */
+PKV_API pkv_status pkv_append(pkv_pool* pool, const int32_t* seqs, int32_t n, int64_t* slots_out,
+                      int32_t* cow_pairs_out, int32_t* n_cow_out);
+
+/* New sequence sharing every block of parent (each block's refcount + 1); takes the lowest
+ * unused id. Errors: NO_SEQ, CAPACITY. */
+PKV_API pkv_status pkv_fork(pkv_pool* pool, int32_t parent, int32_t* child_out);
+
+/* Release seq: every block of its table, in table order, loses one reference; a block that
+ * reaches zero goes on top of the free list. Blocks still referenced elsewhere stay in use. */
+PKV_API pkv_status pkv_free(pkv_pool* pool, int32_t seq);
+
+/* Host copies of the block tables of n live sequences: table_out[n][max_blocks_per_seq]
+ * (int32, unused entries -1) and lens_out[n]. Either output may be NULL. */
+PKV_API pkv_status pkv_block_table(const pkv_pool* pool, const int32_t* seqs, int32_t n, int32_t* table_out,
+                           int32_t* lens_out);
+
+PKV_API pkv_status pkv_pool_stats(const pkv_pool* pool, pkv_stats* out);
+
+/* Allocator state for checking: refcounts[NB]; free_list[NB] from the bottom of the stack to its
+ * top (the top is handed out next), first *n_free entries valid. */
+PKV_API pkv_status pkv_export_state(const pkv_pool* pool, int32_t* refcounts, int32_t* free_list, int32_t* n_free);
+
+/* ---- device operations -------------------------------------------------------------------- */
+/* All pointers below are device pointers unless marked host; they must be 16-byte aligned.
+ * Host-side argument errors return PKV_ERR_INVALID before anything is enqueued; a failed launch
+ * returns PKV_ERR_CUDA. Kernels never fault on bad block ids or slots: they skip the access and
+ * record PKV_ERR_DEVICE_BOUNDS for pkv_last_error. */
+
+/* Slot-mapped append of new K/V (bit copy, no conversion): for each token i with slot s = slots[i]
+ * (s < 0: skipped), for every KV head h: k_cache[s/B][h][s%B][:] = k[i][h][:], same for V.
+ * k, v: [n_tokens][Hkv][D] in the pool dtype; slots: int64 [n_tokens]; caches: one layer. */
+PKV_API pkv_status pkv_reshape_and_cache(const pkv_pool* pool, const void* k, const void* v, const int64_t* slots,
+                                 int32_t n_tokens, void* k_cache, void* v_cache, void* stream);
+
+/* Copy-on-write block copies for every layer: for l < num_layers and each pair i (in order),
+ * k_caches[l][dst_i] = k_caches[l][src_i] and the same for V (a whole block: Hkv * B * D values).
+ * k_caches, v_caches: HOST arrays of num_layers device pointers; pairs: device int32 [n_pairs][2]
+ * (src, dst). A dst must not also be a src in the same call (the allocator never emits that). */
+PKV_API pkv_status pkv_copy_blocks(const pkv_pool* pool, void* const* k_caches, void* const* v_caches,
+                           const int32_t* pairs, int32_t n_pairs, void* stream);
+
+/* Paged decode attention for one layer. For each sequence b < n_seqs and query head j < num_q_heads
+ * (num_q_heads a multiple of Hkv; KV head h = j / (num_q_heads / Hkv)):
+ *     out[b][j][:] = sum_{t < len_b} softmax_t(scale * q[b][j] . K_b[t]) V_b[t]
+ * where K_b[t] = k_cache[block_tables[b][t / B]][h][t % B][:] and len_b = context_lens[b] (the
+ * length includes the token appended in this step; len_b == 0 gives a zero row).
+ * q: [n_seqs][num_q_heads][D] pool dtype; out: float32 [n_seqs][num_q_heads][D];
+ * block_tables: int32 [n_seqs][max_blocks_per_seq]; context_lens: int32 [n_seqs], each at most
+ * max_blocks_per_seq * B.
+ * partition_tokens = 0: the library splits the total work evenly over the GPU (whole 16-token
+ * chunks) and merges split sequences with a log-sum-exp reduce. partition_tokens > 0 (a multiple
+ * of 16): every sequence is cut into partitions of that many tokens, each computed separately and
+ * merged by the same reduce. The result never depends on where blocks are placed physically.
+ * workspace: device scratch of at least pkv_decode_workspace_bytes(...) bytes (may be NULL if that
+ * is 0); its contents need no initialisation. Concurrent calls must not share a workspace. */
+PKV_API pkv_status pkv_paged_decode(const pkv_pool* pool, float* out, const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                            int32_t n_seqs, int32_t num_q_heads, float scale, int32_t partition_tokens,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes pkv_paged_decode needs for these arguments on the current device. */
+PKV_API size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t n_seqs, int32_t num_q_heads,
+                                  int32_t partition_tokens);
+
+/* Synchronise the current device, then return and clear the error recorded by kernels
+ * (PKV_ERR_DEVICE_BOUNDS / PKV_ERR_DEVICE_TIMEOUT), PKV_ERR_CUDA if the device reports an error,
+ * else PKV_OK. pool may be NULL. */
+PKV_API pkv_status pkv_last_error(const pkv_pool* pool);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

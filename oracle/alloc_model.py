@@ -121,6 +121,40 @@ class PoolModel:
         self.n_allocs += 1
         return OK, sid, slots, pairs
 
+    def append(self, seqs: Sequence[int]) -> Tuple[int, List[int], List[Tuple[int, int]]]:
+        """One decode step: one position for each listed sequence, in order, all or nothing.
+
+        Returns (status, slots, cow_pairs). Duplicate ids are invalid."""
+        seqs = [int(s) for s in seqs]
+        if len(set(seqs)) != len(seqs):
+            return ERR_INVALID, [], []
+        if any(s not in self.tables for s in seqs):
+            return ERR_NO_SEQ, [], []
+        if any(-(-(self.lens[s] + 1) // self.B) > self.MB for s in seqs):
+            return ERR_CAPACITY, [], []
+        if self.fail_after >= 0 and self.n_allocs >= self.fail_after:
+            return ERR_NO_BLOCKS, [], []
+        # count the blocks the step needs by replaying it on a scratch copy of the refcounts
+        rc = list(self.refcount)
+        need = 0
+        for s in seqs:
+            if self.lens[s] % self.B == 0:
+                need += 1
+            elif rc[self.tables[s][-1]] > 1:
+                rc[self.tables[s][-1]] -= 1
+                need += 1
+        if need > len(self.free):
+            return ERR_NO_BLOCKS, [], []
+        slots, pairs = [], []
+        for s in seqs:
+            st, _, sl, pr = self.alloc(s, 1)
+            assert st == OK
+            self.n_allocs -= 1
+            slots += sl
+            pairs += pr
+        self.n_allocs += 1
+        return OK, slots, pairs
+
     def fork(self, parent: int) -> Tuple[int, int]:
         """New sequence sharing every block of ``parent`` (refcount + 1 each). Returns (status, child)."""
         if parent not in self.tables:

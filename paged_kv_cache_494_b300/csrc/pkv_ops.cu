@@ -1,0 +1,253 @@
+// Device-operation entry points of libpagedkv (C ABI, see include/pagedkv.h): argument checks,
+// launch planning, workspace layout and kernel dispatch. All device code lives in this
+// translation unit (kernels_*.cuh are included here only).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "kernels_cache.cuh"
+#include "kernels_decode.cuh"
+#include "pkv_pool.hpp"
+
+namespace {
+
+using pkv_dev::DecodeArgs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cached[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+int env_int(const char* name, int fallback) {
+  const char* s = std::getenv(name);
+  if (!s || !*s) return fallback;
+  const int v = std::atoi(s);
+  return v > 0 ? v : fallback;
+}
+
+// ---------------------------------------------------------------------------------------------
+// decode planning
+// ---------------------------------------------------------------------------------------------
+using DecodeKernel = void (*)(DecodeArgs);
+
+struct KernelPair {
+  DecodeKernel decode = nullptr;
+  DecodeKernel reduce = nullptr;
+  int chunk_bytes = 0;
+};
+
+template <typename T, int D, int G>
+KernelPair pair_for() {
+  KernelPair k;
+  k.decode = pkv_dev::paged_decode_simt_kernel<T, D, G>;
+  k.reduce = pkv_dev::decode_reduce_kernel<D, G>;
+  k.chunk_bytes = pkv_dev::SimtShape<T, D, G>::CB;
+  return k;
+}
+
+template <typename T, int D>
+KernelPair pick_g(int g) {
+  switch (g) {
+    case 1: return pair_for<T, D, 1>();
+    case 2: return pair_for<T, D, 2>();
+    case 3: return pair_for<T, D, 3>();
+    case 4: return pair_for<T, D, 4>();
+    case 5: return pair_for<T, D, 5>();
+    case 6: return pair_for<T, D, 6>();
+    case 8: return pair_for<T, D, 8>();
+    default: return KernelPair{};
+  }
+}
+
+KernelPair pick_kernels(int dtype, int D, int g) {
+  if (dtype == PKV_F32) {
+    if (D == 64) return pick_g<float, 64>(g);
+    if (D == 128) return pick_g<float, 128>(g);
+  } else if (dtype == PKV_BF16) {
+    if (D == 64) return pick_g<__nv_bfloat16, 64>(g);
+    if (D == 128) return pick_g<__nv_bfloat16, 128>(g);
+  }
+  return KernelPair{};
+}
+
+struct DecodePlan {
+  KernelPair k;
+  int nw = 4, stages = 2, grid = 0, warps = 0;
+  size_t smem = 0;
+  int part_chunks = 0, max_parts = 0;
+  int64_t n_units = 0, n_slots = 0;
+  size_t off_ml = 0, off_o = 0, ws_bytes = 0;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t partition_tokens, DecodePlan* out) {
+  const pkv_pool_desc& d = p->desc;
+  if (n_seqs < 0 || Hq <= 0 || Hq % d.num_kv_heads != 0) return PKV_ERR_INVALID;
+  if (d.block_size % pkv_dev::kChunk != 0) return PKV_ERR_INVALID;
+  if (partition_tokens < 0 || partition_tokens % pkv_dev::kChunk != 0) return PKV_ERR_INVALID;
+  if (n_seqs > 16384) return PKV_ERR_INVALID;
+  const int g = Hq / d.num_kv_heads;
+  DecodePlan pl;
+  pl.k = pick_kernels(d.dtype, d.head_dim, g);
+  if (!pl.k.decode) return PKV_ERR_INVALID;
+  pl.nw = env_int("PKV_DECODE_WARPS", 4);
+  pl.stages = env_int("PKV_DECODE_STAGES", 2);
+  pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.chunk_bytes, n_seqs);
+  if (cudaFuncSetAttribute(pl.k.decode, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
+      cudaSuccess)
+    return PKV_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pl.k.decode, pl.nw * 32, pl.smem) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  const int sms = num_sms();
+  if (per_sm <= 0 || sms <= 0) return PKV_ERR_CUDA;
+  pl.grid = sms * per_sm;
+  pl.warps = pl.grid * pl.nw;
+  pl.n_units = static_cast<int64_t>(n_seqs) * d.num_kv_heads;
+  if (partition_tokens > 0) {
+    pl.part_chunks = partition_tokens / pkv_dev::kChunk;
+    const int64_t max_chunks = (static_cast<int64_t>(d.max_blocks_per_seq) * d.block_size) / pkv_dev::kChunk;
+    pl.max_parts = static_cast<int>((max_chunks + pl.part_chunks - 1) / pl.part_chunks);
+    pl.n_slots = pl.n_units * pl.max_parts;
+  } else {
+    pl.n_slots = 2 * static_cast<int64_t>(pl.warps);
+  }
+  const size_t desc_bytes = partition_tokens > 0 ? 0 : static_cast<size_t>(pl.n_units) * 2 * sizeof(int32_t);
+  pl.off_ml = round_up(desc_bytes, 256);
+  pl.off_o = pl.off_ml + round_up(static_cast<size_t>(pl.n_slots) * g * 2 * sizeof(float), 256);
+  pl.ws_bytes = pl.off_o + static_cast<size_t>(pl.n_slots) * g * d.head_dim * sizeof(float);
+  *out = pl;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_reshape_and_cache(const pkv_pool* p, const void* k, const void* v, const int64_t* slots,
+                                 int32_t n_tokens, void* k_cache, void* v_cache, void* stream) {
+  if (!p || n_tokens < 0) return PKV_ERR_INVALID;
+  if (n_tokens == 0) return PKV_OK;
+  if (!k || !v || !slots || !k_cache || !v_cache) return PKV_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(slots) & 7u))
+    return PKV_ERR_INVALID;
+  const pkv_pool_desc& d = p->desc;
+  const int row_bytes = d.head_dim * pkv::elem_bytes(d.dtype);
+  if (row_bytes % 16 != 0) return PKV_ERR_INVALID;
+  const int ppr = row_bytes / 16;
+  const int64_t total = static_cast<int64_t>(n_tokens) * d.num_kv_heads * ppr;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int grid = static_cast<int>(want < 65535 * 4 ? want : 65535 * 4);
+  pkv_dev::reshape_and_cache_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, n_tokens, d.num_kv_heads, ppr,
+      d.block_size, static_cast<int64_t>(d.num_blocks) * d.block_size, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache));
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks(const pkv_pool* p, void* const* k_caches, void* const* v_caches, const int32_t* pairs,
+                           int32_t n_pairs, void* stream) {
+  if (!p || n_pairs < 0) return PKV_ERR_INVALID;
+  if (n_pairs == 0) return PKV_OK;
+  const pkv_pool_desc& d = p->desc;
+  if (!k_caches || !v_caches || !pairs || d.num_layers > pkv_dev::kMaxLayers) return PKV_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(pairs) & 7u) return PKV_ERR_INVALID;
+  pkv_dev::LayerCaches lc;
+  std::memset(&lc, 0, sizeof lc);
+  for (int l = 0; l < d.num_layers; ++l) {
+    if (!k_caches[l] || !v_caches[l] || !aligned16(k_caches[l]) || !aligned16(v_caches[l])) return PKV_ERR_INVALID;
+    lc.k[l] = static_cast<uint4*>(k_caches[l]);
+    lc.v[l] = static_cast<uint4*>(v_caches[l]);
+  }
+  const int64_t block_bytes =
+      static_cast<int64_t>(d.num_kv_heads) * d.block_size * d.head_dim * pkv::elem_bytes(d.dtype);
+  if (block_bytes % 16 != 0) return PKV_ERR_INVALID;
+  const int64_t grid = static_cast<int64_t>(n_pairs) * d.num_layers;
+  if (grid > 0x7fffffff) return PKV_ERR_INVALID;
+  pkv_dev::copy_blocks_kernel<<<static_cast<unsigned>(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      lc, pairs, d.num_layers, block_bytes / 16, d.num_blocks);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_pool* p, int32_t n_seqs, int32_t num_q_heads, int32_t partition_tokens) {
+  if (!p) return 0;
+  DecodePlan pl;
+  if (plan_decode(p, n_seqs, num_q_heads, partition_tokens, &pl) != PKV_OK) return 0;
+  return pl.ws_bytes;
+}
+
+pkv_status pkv_paged_decode(const pkv_pool* p, float* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens, int32_t n_seqs,
+                            int32_t num_q_heads, float scale, int32_t partition_tokens, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!p) return PKV_ERR_INVALID;
+  if (n_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return PKV_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID;
+  DecodePlan pl;
+  const pkv_status st = plan_decode(p, n_seqs, num_q_heads, partition_tokens, &pl);
+  if (st != PKV_OK) return st;
+  if (workspace_bytes < pl.ws_bytes || (pl.ws_bytes > 0 && (!workspace || !aligned16(workspace))))
+    return PKV_ERR_INVALID;
+  const pkv_pool_desc& d = p->desc;
+  DecodeArgs a;
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  a.ws_desc = reinterpret_cast<int32_t*>(ws);
+  a.ws_ml = reinterpret_cast<float*>(ws + pl.off_ml);
+  a.ws_o = reinterpret_cast<float*>(ws + pl.off_o);
+  a.n_seqs = n_seqs;
+  a.Hq = num_q_heads;
+  a.Hkv = d.num_kv_heads;
+  a.B = d.block_size;
+  a.NB = d.num_blocks;
+  a.MB = d.max_blocks_per_seq;
+  a.part_chunks = pl.part_chunks;
+  a.max_parts = pl.max_parts;
+  a.stages = pl.stages;
+  a.total_warps = pl.warps;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  pl.k.decode<<<pl.grid, pl.nw * 32, pl.smem, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  const int64_t units = pl.n_units;
+  if (units > 0x7fffffff) return PKV_ERR_INVALID;
+  pl.k.reduce<<<static_cast<unsigned>(units), 128, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_last_error(const pkv_pool*) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+  unsigned int bits = 0;
+  if (cudaMemcpyFromSymbol(&bits, pkv_dev::g_error_bits, sizeof bits) != cudaSuccess) return PKV_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (bits && cudaMemcpyToSymbol(pkv_dev::g_error_bits, &zero, sizeof zero) != cudaSuccess) return PKV_ERR_CUDA;
+  if (bits & pkv_dev::ERRBIT_TIMEOUT) return PKV_ERR_DEVICE_TIMEOUT;
+  if (bits & pkv_dev::ERRBIT_BOUNDS) return PKV_ERR_DEVICE_BOUNDS;
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,139 @@
+"""Paged decode on the GPU against the binary64 oracle on the same seeded inputs.
+
+Tolerances (max abs error): 2e-3 for bf16 K/V with fp32 accumulation, 1e-5 for fp32.
+Each side built its own block tables and caches (see gpu_cases.Case).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_494_b300 as pkv
+import synth
+from tests.gpu_cases import TOL, Case, case_from_workload, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def check(c: Case, out: torch.Tensor, ref=None):
+    ref = c.oracle_decode() if ref is None else ref
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    assert err <= TOL[c.dtype], err
+    return err
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "gqa5_bf16", "prefix_cow_bf16", "prefix_cow_partial_bf16"])
+@pytest.mark.parametrize("partition_tokens", [0, 512, 64])
+def test_workload_parity(name, partition_tokens):
+    c = case_from_workload(name)
+    check(c, c.gpu_decode(partition_tokens))
+    assert pkv.last_error() == pkv.OK
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 8])
+def test_shapes_and_ragged_tails(dtype, D, G):
+    lens = [0, 1, 2, 15, 16, 17, 33, 100, 257, 700]
+    c = Case(lengths=lens, Hq=2 * G, Hkv=2, D=D, B=32 if G % 2 else 16, dtype=dtype, seed=G)
+    for pt in (0, 32):
+        out = c.gpu_decode(pt)
+        check(c, out)
+        assert torch.all(out[0] == 0)             # empty context gives a zero row
+    assert pkv.last_error() == pkv.OK
+
+
+def test_single_token_returns_v_row():
+    c = Case(lengths=[1, 1, 1], Hq=8, Hkv=2, D=128, B=16, dtype="bf16", seed=5)
+    out = c.gpu_decode()
+    for b in range(3):
+        blk = int(c.oracle_tables[b, 0])
+        for j in range(8):
+            v = c.hv[blk, j // 4, 0].astype(np.uint32) << 16
+            assert np.array_equal(out[b, j].cpu().numpy(), v.view(np.float32))
+
+
+def test_extreme_logits_stay_finite():
+    c = Case(lengths=[300, 7, 1000], Hq=8, Hkv=2, D=128, B=16, dtype="bf16", seed=13)
+    q = (torch.from_numpy(synth.bf16_bits_to_f32(c.q_stored)) * 100.0)
+    q_stored = synth.to_bf16_bits(q.numpy())
+    c.q_stored = q_stored
+    out = c.gpu_decode(q=to_device(q_stored, "bf16"))
+    check(c, out)
+
+
+def test_permutation_invariance_bitwise():
+    lens = [5, 300, 1, 77, 1024, 16]
+    c1 = Case(lengths=lens, Hq=32, Hkv=8, D=128, B=16, dtype="bf16", seed=21, num_blocks=200)
+    c2 = Case(lengths=lens, Hq=32, Hkv=8, D=128, B=16, dtype="bf16", seed=21, num_blocks=200,
+              free_list=synth.free_list(200, 999))
+    assert not np.array_equal(c1.oracle_tables, c2.oracle_tables)
+    for pt in (0, 128):
+        assert torch.equal(c1.gpu_decode(pt), c2.gpu_decode(pt))
+
+
+def test_shared_prefix_equals_duplicated_bitwise():
+    """Same logical data: prefix pages shared through forks vs private copies written separately."""
+    B, H, D = 16, 8, 128
+    shared = Case(lengths=[48], Hq=32, Hkv=H, D=D, B=B, dtype="bf16", seed=31, num_blocks=64, max_blocks=8)
+    child = shared.pool.fork(shared.seqs[0])
+    st, mchild = shared.model.fork(shared.seqs[0])
+    assert mchild == child
+    tables, lens = shared.pool.block_table([shared.seqs[0], child])
+    assert tables[0, :3].tolist() == tables[1, :3].tolist()
+    spare = [b for b in range(64) if b not in set(tables[0].tolist())][:3]
+    dup_tables = tables.copy()
+    dup_tables[1, :3] = spare
+    for i, dst in enumerate(spare):                      # private copies of the same pages
+        shared.k_cache[dst] = shared.k_cache[int(tables[0, i])]
+        shared.v_cache[dst] = shared.v_cache[int(tables[0, i])]
+    q = torch.cat([shared.q, shared.q])
+    shared.n = 2
+    lens_d = torch.from_numpy(lens).cuda()
+    a = shared.gpu_decode(q=q, tables=torch.from_numpy(tables).cuda(), lens=lens_d)
+    b = shared.gpu_decode(q=q, tables=torch.from_numpy(dup_tables).cuda(), lens=lens_d)
+    assert torch.equal(a, b)
+    assert torch.equal(a[0], a[1])
+
+
+def test_decode_steps_append_then_attend():
+    c = Case(lengths=[1, 15, 16, 200, 0, 33], Hq=32, Hkv=8, D=128, B=16, dtype="bf16", seed=41, num_blocks=80)
+    for step in range(18):
+        c.decode_step_append()
+        if step % 6 == 5:
+            check(c, c.gpu_decode())
+    assert pkv.last_error() == pkv.OK
+
+
+def test_bad_block_id_reported_not_faulted():
+    c = Case(lengths=[40, 40], Hq=8, Hkv=2, D=128, B=16, dtype="bf16", seed=51)
+    bad = c.tables.clone()
+    bad[1, 1] = c.NB + 5
+    out = c.gpu_decode(tables=bad)
+    assert pkv.last_error() == pkv.ERR_DEVICE_BOUNDS
+    ref = c.oracle_decode()
+    assert np.max(np.abs(out[0].double().cpu().numpy() - ref[0])) <= 2e-3   # untouched sequence is right
+    too_long = c.lens.clone()
+    too_long[0] = c.MB * c.B + 100
+    c.gpu_decode(lens=too_long)
+    assert pkv.last_error() == pkv.ERR_DEVICE_BOUNDS
+    assert pkv.last_error() == pkv.OK
+
+
+def test_host_argument_checks():
+    c = Case(lengths=[40], Hq=8, Hkv=2, D=128, B=16, dtype="bf16", seed=61)
+    out = torch.zeros(1, 8, 128, device="cuda")
+    with pytest.raises(pkv.PagedKVError) as e:           # workspace too small
+        c.pool.paged_decode(out, c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale,
+                            workspace=torch.zeros(4, device="cuda"))
+    assert e.value.status == pkv.ERR_INVALID
+    q7 = torch.zeros(1, 7, 128, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(pkv.PagedKVError):                # 7 query heads over 2 KV heads
+        c.pool.paged_decode(out, q7, c.k_cache, c.v_cache, c.tables, c.lens, c.scale)
+    with pytest.raises(pkv.PagedKVError):                # partition not a multiple of 16
+        c.pool.paged_decode(out, c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, partition_tokens=24)
+    odd = pkv.Pool(1, 2, 128, 8, 16, 2, 8, pkv.BF16)     # block size 8 is not supported by the kernels
+    assert odd.decode_workspace_bytes(1, 8) == 0
