@@ -14,9 +14,11 @@
 //    takes an equal contiguous share of that list (balanced mode), or an equal share of whole
 //    partitions of `part_chunks` chunks (fixed-partition mode). A warp therefore serves one GQA group
 //    per chunk: all G query heads of the KV head use each staged K/V chunk once.
-//  * Per warp, a ring of `stages` shared-memory slots is filled by 1-D TMA bulk copies (one for K,
-//    one for V, 16*D*sizeof(T) bytes each) that complete on an mbarrier; lane 0 issues them
-//    `stages` chunks ahead of the compute.
+//  * Per warp, a ring of `stages` shared-memory slots is filled by TMA copies that complete on an
+//    mbarrier; lane 0 issues them `stages` chunks ahead of the compute. The bf16 path uses 2-D
+//    tensor copies with 128-byte swizzle (16 rows x 128 bytes per box) so that ldmatrix reads are
+//    free of bank conflicts, and computes q.K and p.V with mma.sync (m16n8k16, fp32 accumulate);
+//    the fp32 path uses 1-D bulk copies and CUDA-core dot products with warp shuffles.
 //  * A segment is the part of a unit one warp processes. A segment that is a whole unit writes the
 //    output directly; otherwise it writes (m, l, o/l) to the workspace and the reduce kernel merges
 //    the segments of the unit: M = max m_k, w_k = l_k 2^(m_k - M), o = sum w_k o_k / sum w_k.
@@ -32,6 +34,12 @@
 namespace pkv_dev {
 
 constexpr int kChunk = 16;  // tokens per staged chunk
+
+// Tensor maps of the K and V caches viewed as 2-D [rows = NB*Hkv*B][D] bf16 arrays.
+struct TmaMaps {  // CUtensorMap is itself 64-byte aligned
+  CUtensorMap k;
+  CUtensorMap v;
+};
 
 struct DecodeArgs {
   float* out;                    // [n_seqs][Hq][D]
@@ -110,12 +118,13 @@ __device__ __forceinline__ int64_t item_start(const int32_t* pref, const int32_t
   return static_cast<int64_t>(pref[b]) * Hkv + static_cast<int64_t>(h) * nch + static_cast<int64_t>(p) * PC;
 }
 
-// Shared-memory carve-up of the decode kernel. Ring first (each stage: K chunk then V chunk).
-__host__ __device__ inline size_t decode_ring_bytes(int nw, int stages, int chunk_bytes) {
-  return static_cast<size_t>(nw) * stages * 2 * chunk_bytes;
+// Shared-memory carve-up of the decode kernel: [1 KB alignment slack][ring: per warp `stages` stages]
+// [mbarriers][prefix arrays]. Stages start on 1024-byte boundaries (128-byte swizzle atoms).
+__host__ __device__ inline size_t decode_ring_bytes(int nw, int stages, int stage_bytes) {
+  return static_cast<size_t>(nw) * stages * stage_bytes;
 }
-__host__ __device__ inline size_t decode_smem_bytes(int nw, int stages, int chunk_bytes, int n_seqs) {
-  return decode_ring_bytes(nw, stages, chunk_bytes) + static_cast<size_t>(nw) * stages * 8 +
+__host__ __device__ inline size_t decode_smem_bytes(int nw, int stages, int stage_bytes, int n_seqs) {
+  return 1024 + decode_ring_bytes(nw, stages, stage_bytes) + static_cast<size_t>(nw) * stages * 8 +
          2 * static_cast<size_t>(n_seqs + 1) * 4;
 }
 
@@ -156,11 +165,13 @@ __device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref,
 }
 
 // ------------------------------------------------------------------------------------------------
-// SIMT decode: CUDA-core dot products with warp shuffles. Lane layout: LPT lanes per token, each
-// holding EPL consecutive-by-piece elements of the head dimension; TPP tokens per pass.
+// SIMT math: CUDA-core dot products with warp shuffles (fp32 caches, and bf16 when G > 8).
+// Lane layout: LPT lanes per token, each holding EPL elements of the head dimension (PIECES
+// 16-byte pieces spaced LPT pieces apart, so a quarter-warp reads 128 contiguous bytes);
+// TPP tokens per pass. Scores are pre-scaled into log2 units through q.
 // ------------------------------------------------------------------------------------------------
 template <typename T, int D, int G>
-struct SimtShape {
+struct SimtMath {
   static constexpr int es = sizeof(T);
   static constexpr int PER16 = Widen<T>::kPer16;
   static constexpr int EPL = (G <= 5) ? 16 : 8;
@@ -169,16 +180,303 @@ struct SimtShape {
   static constexpr int PASSES = kChunk / TPP;
   static constexpr int PIECES = EPL / PER16;
   static constexpr int CB = kChunk * D * es;  // bytes of one K (or V) chunk
+  static constexpr int kStageBytes = 2 * CB;
   static_assert(LPT * EPL == D && TPP * LPT == 32 && PASSES * TPP == kChunk, "lane layout");
   static_assert(PIECES * PER16 == EPL, "pieces");
+
+  struct Regs {
+    float q[G][EPL];
+    float o[G][EPL];
+    float m[G], l[G];
+  };
+
+  // lane 0: stage the chunk starting at cache row `row0` (= (blk*Hkv + h)*B + offset)
+  __device__ static void issue(const DecodeArgs& a, const TmaMaps&, uint32_t dst, uint32_t bar, int64_t row0,
+                               uint64_t policy) {
+    mbar_arrive_expect_tx(bar, 2 * CB);
+    const int64_t byte0 = row0 * D * es;
+    bulk_g2s_hint(dst, static_cast<const unsigned char*>(a.k_cache) + byte0, CB, bar, policy);
+    bulk_g2s_hint(dst + CB, static_cast<const unsigned char*>(a.v_cache) + byte0, CB, bar, policy);
+  }
+
+  __device__ static void load_q(Regs& r, const DecodeArgs& a, int32_t b, int32_t h, int lane) {
+    const int cl = lane % LPT;
+    const T* qbase = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * G) * D;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+#pragma unroll
+      for (int i = 0; i < PIECES; ++i) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qbase + j * D + (cl + i * LPT) * PER16));
+        Widen<T>::load(reinterpret_cast<const unsigned char*>(&raw), &r.q[j][i * PER16]);
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) r.q[j][e] *= a.scale_log2;
+    }
+  }
+
+  __device__ static void reset(Regs& r) {
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      r.m[j] = -INFINITY;
+      r.l[j] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) r.o[j][e] = 0.f;
+    }
+  }
+
+  __device__ static void chunk(Regs& r, const unsigned char* kb, int nvalid, float, int lane) {
+    const unsigned char* vb = kb + CB;
+    const int tg = lane / LPT;
+    const int cl = lane % LPT;
+    float sc[PASSES][G];
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int tok = p * TPP + tg;
+      float kf[EPL];
+#pragma unroll
+      for (int pc = 0; pc < PIECES; ++pc)
+        Widen<T>::load(kb + (tok * D + (cl + pc * LPT) * PER16) * es, kf + pc * PER16);
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) s = fmaf(r.q[j][e], kf[e], s);
+#pragma unroll
+        for (int off = LPT / 2; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        sc[p][j] = tok < nvalid ? s : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      float mx = sc[0][j];
+#pragma unroll
+      for (int p = 1; p < PASSES; ++p) mx = fmaxf(mx, sc[p][j]);
+#pragma unroll
+      for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mnew = fmaxf(r.m[j], mx);
+      const float alpha = exp2f(r.m[j] - mnew);
+      r.m[j] = mnew;
+      if (alpha != 1.f) {
+        r.l[j] *= alpha;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) r.o[j][e] *= alpha;
+      }
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        sc[p][j] = exp2f(sc[p][j] - mnew);
+        r.l[j] += sc[p][j];
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+      const int tok = p * TPP + tg;
+      if (tok < nvalid) {   // values past the context may be garbage (even NaN): never touch them
+        float vf[EPL];
+#pragma unroll
+        for (int pc = 0; pc < PIECES; ++pc)
+          Widen<T>::load(vb + (tok * D + (cl + pc * LPT) * PER16) * es, vf + pc * PER16);
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) r.o[j][e] = fmaf(sc[p][j], vf[e], r.o[j][e]);
+      }
+    }
+  }
+
+  // Writes o / l for the G heads to dst[G][D]; if ml != nullptr also (m, l) to ml[G][2].
+  __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
+    const int tg = lane / LPT;
+    const int cl = lane % LPT;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      float lt = r.l[j];
+#pragma unroll
+      for (int off = LPT; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        float t = r.o[j][e];
+#pragma unroll
+        for (int off = LPT; off < 32; off <<= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        r.o[j][e] = t;
+      }
+      if (j % TPP != tg) continue;
+      const float inv = 1.f / lt;
+#pragma unroll
+      for (int pc = 0; pc < PIECES; ++pc) {
+        float4* d4 = reinterpret_cast<float4*>(dst + j * D + (cl + pc * LPT) * PER16);
+#pragma unroll
+        for (int k4 = 0; k4 < PER16 / 4; ++k4) {
+          const float* src = &r.o[j][pc * PER16 + 4 * k4];
+          d4[k4] = make_float4(src[0] * inv, src[1] * inv, src[2] * inv, src[3] * inv);
+        }
+      }
+      if (ml != nullptr && cl == 0) {
+        ml[2 * j] = r.m[j];
+        ml[2 * j + 1] = lt;
+      }
+    }
+  }
 };
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
-  using Sh = SimtShape<T, D, G>;
-  constexpr int es = Sh::es, PER16 = Sh::PER16, EPL = Sh::EPL, LPT = Sh::LPT, TPP = Sh::TPP;
-  constexpr int PASSES = Sh::PASSES, PIECES = Sh::PIECES, CB = Sh::CB;
+// ------------------------------------------------------------------------------------------------
+// Tensor-core math for bf16 caches, G <= 8 query heads per KV head.
+//
+// S = Q K^T per 16-token chunk: A = Q (rows = the G heads, zero-padded to 16), B = K chunk read
+// with ldmatrix from the swizzled boxes, fp32 accumulate: 2 n-tiles x D/16 k-steps of m16n8k16.
+// O += P V: A rows 0..7 hold P rounded to bf16 (hi) and rows 8..15 hold the rounding remainder
+// (lo = bf16(P - hi)), so one mma accumulates both and hi + lo carries P to ~2^-17 relative;
+// B = V chunk read with ldmatrix.trans. Lane (g = lane/4, t = lane%4) owns head g, tokens
+// {2t, 2t+1, 8+2t, 9+2t} of each chunk and output dims {8n + 2t, 8n + 2t + 1}.
+// The running max is raised only when a chunk's max exceeds it by more than kRescaleLog2 (the
+// exponentials then stay below 2^kRescaleLog2), which skips most rescales of O without changing
+// the result: numerator and denominator always use the same max.
+// ------------------------------------------------------------------------------------------------
+template <int D, int G>
+struct MmaMath {
+  static_assert(G >= 1 && G <= 8, "G <= 8");
+  static_assert(D == 64 || D == 128, "D");
+  static constexpr int KB = D / 64;          // 128-byte boxes per row
+  static constexpr int BOX = kChunk * 128;   // one box: 16 rows x 128 bytes
+  static constexpr int CB = KB * BOX;        // K (or V) chunk bytes
+  static constexpr int kStageBytes = 2 * CB;
+  static constexpr int KS = D / 16;          // k-steps of q.K
+  static constexpr int NT = D / 8;           // n-tiles of p.V
+  static constexpr float kRescaleLog2 = 8.f;
 
+  struct Regs {
+    uint32_t qa[KS][2];  // A fragment registers 0 and 2 (rows 8..15 are zero)
+    float o[NT][4];      // [0..1]: hi part (row g), [2..3]: lo part (row g + 8)
+    float m, l;          // running max (log2 units) and this lane's share of the sum, head g
+  };
+
+  __device__ static void issue(const DecodeArgs&, const TmaMaps& maps, uint32_t dst, uint32_t bar, int64_t row0,
+                               uint64_t policy) {
+    mbar_arrive_expect_tx(bar, 2 * CB);
+    const int32_t y = static_cast<int32_t>(row0);
+#pragma unroll
+    for (int kb = 0; kb < KB; ++kb) {
+      tma_load_2d(dst + kb * BOX, &maps.k, 64 * kb, y, bar, policy);
+      tma_load_2d(dst + CB + kb * BOX, &maps.v, 64 * kb, y, bar, policy);
+    }
+  }
+
+  __device__ static void load_q(Regs& r, const DecodeArgs& a, int32_t b, int32_t h, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint32_t* qrow =
+        reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * G + g) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      r.qa[ks][0] = g < G ? __ldg(qrow + 8 * ks + t) : 0u;
+      r.qa[ks][1] = g < G ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+    }
+  }
+
+  __device__ static void reset(Regs& r) {
+    r.m = -INFINITY;
+    r.l = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) r.o[n][0] = r.o[n][1] = r.o[n][2] = r.o[n][3] = 0.f;
+  }
+
+  // Byte offset of 16-byte block `cb` (0..7) of row `row` inside a 128B-swizzled box.
+  __device__ static __forceinline__ uint32_t swz(int row, int cb) {
+    return static_cast<uint32_t>(row * 128 + ((cb ^ (row & 7)) << 4));
+  }
+
+  __device__ static void chunk(Regs& r, const unsigned char* kbase, int nvalid, float scale_log2, int lane) {
+    const uint32_t kb = smem_addr(kbase);
+    const uint32_t vb = kb + CB;
+    const int t = lane & 3;
+    const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix index and row of this lane's address
+    // ---- S = Q K^T
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const int tok = 8 * nt + mr;
+#pragma unroll
+      for (int p = 0; p < KS / 2; ++p) {
+        const int db = 4 * p + mi;                      // 16-byte block of 8 dims
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + (db >> 3) * BOX + swz(tok, db & 7), b0, b1, b2, b3);
+        mma_bf16_16816(s[nt], r.qa[2 * p][0], 0u, r.qa[2 * p][1], 0u, b0, b1);
+        mma_bf16_16816(s[nt], r.qa[2 * p + 1][0], 0u, r.qa[2 * p + 1][1], 0u, b2, b3);
+      }
+    }
+    // ---- online softmax for head g over tokens {2t, 2t+1, 8+2t, 9+2t}
+    float x[4];
+    x[0] = (2 * t < nvalid) ? s[0][0] * scale_log2 : -INFINITY;
+    x[1] = (2 * t + 1 < nvalid) ? s[0][1] * scale_log2 : -INFINITY;
+    x[2] = (8 + 2 * t < nvalid) ? s[1][0] * scale_log2 : -INFINITY;
+    x[3] = (9 + 2 * t < nvalid) ? s[1][1] * scale_log2 : -INFINITY;
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const bool raise = mx > r.m + kRescaleLog2;
+    if (__any_sync(0xffffffffu, raise)) {
+      const float mnew = raise ? mx : r.m;
+      const float alpha = exp2f(r.m - mnew);  // 0 on the first chunk (m = -inf), 1 if unchanged
+      r.m = mnew;
+      r.l *= alpha;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        r.o[n][0] *= alpha;
+        r.o[n][1] *= alpha;
+        r.o[n][2] *= alpha;
+        r.o[n][3] *= alpha;
+      }
+    }
+    float pr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pr[e] = exp2f(x[e] - r.m);
+    r.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    const uint32_t hi0 = pack_bf16x2(pr[0], pr[1]);
+    const uint32_t hi1 = pack_bf16x2(pr[2], pr[3]);
+    const uint32_t lo0 = pack_bf16x2(pr[0] - bf16_lo(hi0), pr[1] - bf16_hi(hi0));
+    const uint32_t lo1 = pack_bf16x2(pr[2] - bf16_lo(hi1), pr[3] - bf16_hi(hi1));
+    // ---- O += P V (rows 0..7: hi, rows 8..15: lo)
+    uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
+    if (nvalid < kChunk) {  // zero V entries of tokens past the context (they may hold NaN)
+      mask01 = ((2 * t < nvalid) ? 0x0000ffffu : 0u) | ((2 * t + 1 < nvalid) ? 0xffff0000u : 0u);
+      mask23 = ((8 + 2 * t < nvalid) ? 0x0000ffffu : 0u) | ((9 + 2 * t < nvalid) ? 0xffff0000u : 0u);
+    }
+    const int vtok = mr + 8 * (mi & 1);
+#pragma unroll
+    for (int pair = 0; pair < NT / 2; ++pair) {
+      const int db = 2 * pair + (mi >> 1);
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vb + (db >> 3) * BOX + swz(vtok, db & 7), v0, v1, v2, v3);
+      mma_bf16_16816(r.o[2 * pair], hi0, lo0, hi1, lo1, v0 & mask01, v1 & mask23);
+      mma_bf16_16816(r.o[2 * pair + 1], hi0, lo0, hi1, lo1, v2 & mask01, v3 & mask23);
+    }
+  }
+
+  __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float lt = r.l;
+    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    if (g >= G) return;
+    const float inv = 1.f / lt;
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+      *reinterpret_cast<float2*>(dst + g * D + 8 * n + 2 * t) =
+          make_float2((r.o[n][0] + r.o[n][2]) * inv, (r.o[n][1] + r.o[n][3]) * inv);
+    if (ml != nullptr && t == 0) {
+      ml[2 * g] = r.m;
+      ml[2 * g + 1] = lt;
+    }
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// The decode kernel: prefix of chunk counts, even split of the flat chunk list over warps, a
+// per-warp TMA ring, segment bookkeeping and output / partial writes. Math is a policy.
+// ------------------------------------------------------------------------------------------------
+template <class Math, int D, int G>
+__global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant__ DecodeArgs a,
+                                                           const __grid_constant__ TmaMaps maps) {
+  constexpr int SB = Math::kStageBytes;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int NW = blockDim.x >> 5;
@@ -186,10 +484,11 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
   const int32_t n = a.n_seqs, Hkv = a.Hkv;
   const int32_t PC = a.part_chunks;
 
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* ring = smem + static_cast<size_t>(warp) * S * 2 * CB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + decode_ring_bytes(NW, S, CB)) + warp * S;
-  int32_t* pref = reinterpret_cast<int32_t*>(smem + decode_ring_bytes(NW, S, CB) + static_cast<size_t>(NW) * S * 8);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  unsigned char* ring = smem + static_cast<size_t>(warp) * S * SB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + decode_ring_bytes(NW, S, SB)) + warp * S;
+  int32_t* pref = reinterpret_cast<int32_t*>(smem + decode_ring_bytes(NW, S, SB) + static_cast<size_t>(NW) * S * 8);
   int32_t* ipref = pref + (n + 1);
 
   if (warp == 0) build_prefix(a, pref, ipref, lane);
@@ -228,10 +527,7 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
   const int64_t n_chunks = hi - lo;
   if (n_chunks <= 0) return;
 
-  const int tg = lane / LPT;  // token group
-  const int cl = lane % LPT;  // piece column
-
-  // --- producer state (lane-uniform except the table window register) ---
+  // --- producer (lane 0 issues; the block-table window is spread over the lanes) ---
   Cursor pf = locate(pref, n, Hkv, lo);
   int32_t win_b = -1, win_base = 0, win_val = -1;
   const uint64_t policy = policy_evict_first();
@@ -250,12 +546,9 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
     if (lane == 0) {
       const uint32_t bar = smem_addr(bars + stage);
       if (blk >= 0 && blk < a.NB) {
-        const int64_t e0 = ((static_cast<int64_t>(blk) * Hkv + pf.h) * a.B + (tok0 - pg * a.B)) * D;
+        const int64_t row0 = (static_cast<int64_t>(blk) * Hkv + pf.h) * a.B + (tok0 - pg * a.B);
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, 2 * CB);
-        const uint32_t dst = smem_addr(ring + static_cast<size_t>(stage) * 2 * CB);
-        bulk_g2s_hint(dst, static_cast<const unsigned char*>(a.k_cache) + e0 * es, CB, bar, policy);
-        bulk_g2s_hint(dst + CB, static_cast<const unsigned char*>(a.v_cache) + e0 * es, CB, bar, policy);
+        Math::issue(a, maps, smem_addr(ring + static_cast<size_t>(stage) * SB), bar, row0, policy);
       } else {
         record_error(ERRBIT_BOUNDS);
         mbar_arrive(bar);  // completes the phase with no data; the chunk's result is garbage
@@ -267,37 +560,12 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
 
   for (int s = 0; s < S && issued < n_chunks; ++s) issue(s);
 
-  // --- consumer state ---
+  // --- consumer ---
   Cursor cc = locate(pref, n, Hkv, lo);
-  float qf[G][EPL];
-  float of[G][EPL];
-  float m[G], l[G];
-  int32_t len_b = 0;
+  typename Math::Regs r;
   int32_t seg_c0 = cc.c;
   int seg_idx = 0;
 
-  auto load_q = [&]() {
-    const T* qbase = static_cast<const T*>(a.q) + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G) * D;
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-#pragma unroll
-      for (int i = 0; i < PIECES; ++i) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qbase + j * D + (cl + i * LPT) * PER16));
-        Widen<T>::load(reinterpret_cast<const unsigned char*>(&raw), &qf[j][i * PER16]);
-      }
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) qf[j][e] *= a.scale_log2;
-    }
-  };
-  auto reset_state = [&]() {
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      m[j] = -INFINITY;
-      l[j] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) of[j][e] = 0.f;
-    }
-  };
   auto write_desc = [&](int64_t x) {  // balanced mode, at the first chunk of a unit
     if (PC != 0 || lane != 0) return;
     const int64_t e_u = x + cc.nch;
@@ -311,9 +579,9 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
     }
   };
 
-  len_b = clamped_len(a, cc.b);
-  load_q();
-  reset_state();
+  int32_t len_b = clamped_len(a, cc.b);
+  Math::load_q(r, a, cc.b, cc.h, lane);
+  Math::reset(r);
   if (cc.c == 0) write_desc(lo);
 
   bool aborted = false;
@@ -325,65 +593,8 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
       aborted = true;
       break;
     }
-    const unsigned char* kb = ring + static_cast<size_t>(stage) * 2 * CB;
-    const unsigned char* vb = kb + CB;
     const int32_t nvalid = min(kChunk, len_b - cc.c * kChunk);
-
-    // scores for this lane's tokens (log2 units), masked beyond the context length
-    float sc[PASSES][G];
-#pragma unroll
-    for (int p = 0; p < PASSES; ++p) {
-      const int tok = p * TPP + tg;
-      float kf[EPL];
-#pragma unroll
-      for (int pc = 0; pc < PIECES; ++pc) Widen<T>::load(kb + (tok * D + (cl + pc * LPT) * PER16) * es, kf + pc * PER16);
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) s = fmaf(qf[j][e], kf[e], s);
-#pragma unroll
-        for (int off = LPT / 2; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        sc[p][j] = tok < nvalid ? s : -INFINITY;
-      }
-    }
-    // online softmax update
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      float mx = sc[0][j];
-#pragma unroll
-      for (int p = 1; p < PASSES; ++p) mx = fmaxf(mx, sc[p][j]);
-#pragma unroll
-      for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mnew = fmaxf(m[j], mx);
-      const float alpha = exp2f(m[j] - mnew);
-      m[j] = mnew;
-      if (alpha != 1.f) {
-        l[j] *= alpha;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) of[j][e] *= alpha;
-      }
-#pragma unroll
-      for (int p = 0; p < PASSES; ++p) {
-        sc[p][j] = exp2f(sc[p][j] - mnew);
-        l[j] += sc[p][j];
-      }
-    }
-    // weighted values
-#pragma unroll
-    for (int p = 0; p < PASSES; ++p) {
-      const int tok = p * TPP + tg;
-      if (tok < nvalid) {
-        float vf[EPL];
-#pragma unroll
-        for (int pc = 0; pc < PIECES; ++pc)
-          Widen<T>::load(vb + (tok * D + (cl + pc * LPT) * PER16) * es, vf + pc * PER16);
-#pragma unroll
-        for (int j = 0; j < G; ++j)
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) of[j][e] = fmaf(sc[p][j], vf[e], of[j][e]);
-      }
-    }
+    Math::chunk(r, ring + static_cast<size_t>(stage) * SB, nvalid, a.scale_log2, lane);
     __syncwarp();
     if (issued < n_chunks) issue(stage);
 
@@ -392,44 +603,14 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
     const bool part_end = (PC != 0) && ((cc.c + 1) % PC == 0);
     const bool range_end = (i + 1 == n_chunks);
     if (unit_end || part_end || range_end) {
-      float lt[G];
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        lt[j] = l[j];
-#pragma unroll
-        for (int off = LPT; off < 32; off <<= 1) lt[j] += __shfl_xor_sync(0xffffffffu, lt[j], off);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-          float t = of[j][e];
-#pragma unroll
-          for (int off = LPT; off < 32; off <<= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-          of[j][e] = t;
-        }
-      }
       const bool complete = (seg_c0 == 0) && unit_end;
       const int64_t u = static_cast<int64_t>(cc.b) * Hkv + cc.h;
-      int64_t slot = 0;
-      if (!complete) slot = (PC == 0) ? (2 * static_cast<int64_t>(w) + (seg_idx == 0 ? 0 : 1))
-                                      : (u * a.max_parts + cc.c / PC);
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        if (j % TPP != tg) continue;
-        const float inv = 1.f / lt[j];
-        float* dst = complete ? a.out + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G + j) * D
-                              : a.ws_o + (slot * G + j) * D;
-#pragma unroll
-        for (int pc = 0; pc < PIECES; ++pc) {
-          float4* d4 = reinterpret_cast<float4*>(dst + (cl + pc * LPT) * PER16);
-#pragma unroll
-          for (int k4 = 0; k4 < PER16 / 4; ++k4) {
-            const float* src = &of[j][pc * PER16 + 4 * k4];
-            d4[k4] = make_float4(src[0] * inv, src[1] * inv, src[2] * inv, src[3] * inv);
-          }
-        }
-        if (!complete && cl == 0) {
-          a.ws_ml[(slot * G + j) * 2] = m[j];
-          a.ws_ml[(slot * G + j) * 2 + 1] = lt[j];
-        }
+      if (complete) {
+        Math::finish(r, a.out + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G) * D, nullptr, lane);
+      } else {
+        const int64_t slot = (PC == 0) ? (2 * static_cast<int64_t>(w) + (seg_idx == 0 ? 0 : 1))
+                                       : (u * a.max_parts + cc.c / PC);
+        Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
       }
       ++seg_idx;
     }
@@ -439,10 +620,10 @@ __global__ void __launch_bounds__(128) paged_decode_simt_kernel(DecodeArgs a) {
       if (unit_end || part_end) {
         if (unit_end) {
           if (cc.b != prev_b) len_b = clamped_len(a, cc.b);
-          load_q();
+          Math::load_q(r, a, cc.b, cc.h, lane);
           if (cc.c == 0) write_desc(lo + i + 1);
         }
-        reset_state();
+        Math::reset(r);
         seg_c0 = cc.c;
       }
     }

@@ -1,6 +1,8 @@
 // Device-operation entry points of libpagedkv (C ABI, see include/pagedkv.h): argument checks,
 // launch planning, workspace layout and kernel dispatch. All device code lives in this
 // translation unit (kernels_*.cuh are included here only).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -8,6 +10,8 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
 
 #include "kernels_cache.cuh"
 #include "kernels_decode.cuh"
@@ -41,46 +45,116 @@ int env_int(const char* name, int fallback) {
 // ---------------------------------------------------------------------------------------------
 // decode planning
 // ---------------------------------------------------------------------------------------------
-using DecodeKernel = void (*)(DecodeArgs);
+using DecodeKernel = void (*)(DecodeArgs, pkv_dev::TmaMaps);
+using ReduceKernel = void (*)(DecodeArgs);
 
 struct KernelPair {
   DecodeKernel decode = nullptr;
-  DecodeKernel reduce = nullptr;
-  int chunk_bytes = 0;
+  ReduceKernel reduce = nullptr;
+  int stage_bytes = 0;
+  bool tensor_maps = false;   // bf16 tensor-core path (K/V staged by 2-D tensor TMA)
 };
 
-template <typename T, int D, int G>
-KernelPair pair_for() {
+template <class Math, int D, int G>
+KernelPair pair_for(bool tmaps) {
   KernelPair k;
-  k.decode = pkv_dev::paged_decode_simt_kernel<T, D, G>;
+  k.decode = pkv_dev::paged_decode_kernel<Math, D, G>;
   k.reduce = pkv_dev::decode_reduce_kernel<D, G>;
-  k.chunk_bytes = pkv_dev::SimtShape<T, D, G>::CB;
+  k.stage_bytes = Math::kStageBytes;
+  k.tensor_maps = tmaps;
   return k;
 }
 
-template <typename T, int D>
-KernelPair pick_g(int g) {
+template <int D, int G>
+KernelPair pick_bf16(bool simt) {
+  if (simt) return pair_for<pkv_dev::SimtMath<__nv_bfloat16, D, G>, D, G>(false);
+  return pair_for<pkv_dev::MmaMath<D, G>, D, G>(true);
+}
+
+template <int D>
+KernelPair pick_g(int dtype, int g, bool simt) {
+  if (dtype == PKV_F32) {
+    switch (g) {
+      case 1: return pair_for<pkv_dev::SimtMath<float, D, 1>, D, 1>(false);
+      case 2: return pair_for<pkv_dev::SimtMath<float, D, 2>, D, 2>(false);
+      case 3: return pair_for<pkv_dev::SimtMath<float, D, 3>, D, 3>(false);
+      case 4: return pair_for<pkv_dev::SimtMath<float, D, 4>, D, 4>(false);
+      case 5: return pair_for<pkv_dev::SimtMath<float, D, 5>, D, 5>(false);
+      case 6: return pair_for<pkv_dev::SimtMath<float, D, 6>, D, 6>(false);
+      case 8: return pair_for<pkv_dev::SimtMath<float, D, 8>, D, 8>(false);
+      default: return KernelPair{};
+    }
+  }
   switch (g) {
-    case 1: return pair_for<T, D, 1>();
-    case 2: return pair_for<T, D, 2>();
-    case 3: return pair_for<T, D, 3>();
-    case 4: return pair_for<T, D, 4>();
-    case 5: return pair_for<T, D, 5>();
-    case 6: return pair_for<T, D, 6>();
-    case 8: return pair_for<T, D, 8>();
+    case 1: return pick_bf16<D, 1>(simt);
+    case 2: return pick_bf16<D, 2>(simt);
+    case 3: return pick_bf16<D, 3>(simt);
+    case 4: return pick_bf16<D, 4>(simt);
+    case 5: return pick_bf16<D, 5>(simt);
+    case 6: return pick_bf16<D, 6>(simt);
+    case 7: return pick_bf16<D, 7>(simt);
+    case 8: return pick_bf16<D, 8>(simt);
     default: return KernelPair{};
   }
 }
 
+// PKV_DECODE_PATH=simt selects the CUDA-core path for bf16 as well (used to cross-check paths).
+bool force_simt() {
+  const char* s = std::getenv("PKV_DECODE_PATH");
+  return s && std::strcmp(s, "simt") == 0;
+}
+
 KernelPair pick_kernels(int dtype, int D, int g) {
-  if (dtype == PKV_F32) {
-    if (D == 64) return pick_g<float, 64>(g);
-    if (D == 128) return pick_g<float, 128>(g);
-  } else if (dtype == PKV_BF16) {
-    if (D == 64) return pick_g<__nv_bfloat16, 64>(g);
-    if (D == 128) return pick_g<__nv_bfloat16, 128>(g);
-  }
+  if (dtype != PKV_F32 && dtype != PKV_BF16) return KernelPair{};
+  const bool simt = force_simt();
+  if (dtype == PKV_F32 && g == 7) return KernelPair{};
+  if (D == 64) return pick_g<64>(dtype, g, simt);
+  if (D == 128) return pick_g<128>(dtype, g, simt);
   return KernelPair{};
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// One cache tensor viewed as a 2-D bf16 array [NB*Hkv*B rows][D], boxes of 16 rows x 64 elements
+// (128 bytes), 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* m, const void* base, const pkv_pool_desc& d) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim),
+                        static_cast<cuuint64_t>(d.num_blocks) * d.num_kv_heads * d.block_size};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pkv_dev::kChunk)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device, size).
+bool ensure_smem(const void* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, size_t> done[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done[dev].find(fn);
+  if (it != done[dev].end() && it->second >= bytes) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
+    return false;
+  done[dev][fn] = bytes;
+  return true;
 }
 
 struct DecodePlan {
@@ -106,10 +180,8 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   if (!pl.k.decode) return PKV_ERR_INVALID;
   pl.nw = env_int("PKV_DECODE_WARPS", 4);
   pl.stages = env_int("PKV_DECODE_STAGES", 2);
-  pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.chunk_bytes, n_seqs);
-  if (cudaFuncSetAttribute(pl.k.decode, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
-      cudaSuccess)
-    return PKV_ERR_CUDA;
+  pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.stage_bytes, n_seqs);
+  if (!ensure_smem(reinterpret_cast<const void*>(pl.k.decode), pl.smem)) return PKV_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pl.k.decode, pl.nw * 32, pl.smem) != cudaSuccess)
     return PKV_ERR_CUDA;
@@ -230,8 +302,15 @@ pkv_status pkv_paged_decode(const pkv_pool* p, float* out, const void* q, const 
   a.stages = pl.stages;
   a.total_warps = pl.warps;
   a.scale_log2 = scale * 1.4426950408889634f;
+  pkv_dev::TmaMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (pl.k.tensor_maps) {
+    const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size;
+    if (rows > 0x7fffffffLL) return PKV_ERR_INVALID;   // tensor coordinates are 32-bit
+    if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d)) return PKV_ERR_CUDA;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  pl.k.decode<<<pl.grid, pl.nw * 32, pl.smem, s>>>(a);
+  pl.k.decode<<<pl.grid, pl.nw * 32, pl.smem, s>>>(a, maps);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   const int64_t units = pl.n_units;
   if (units > 0x7fffffff) return PKV_ERR_INVALID;
