@@ -61,7 +61,8 @@ typedef enum {
   PKV_ERR_CUDA = -4,           /* a CUDA runtime call failed (launch, attribute, device query) */
   PKV_ERR_DEVICE_BOUNDS = -5,  /* a kernel met a block id or slot outside the pool and skipped it */
   PKV_ERR_CAPACITY = -6,       /* max_seqs or max_blocks_per_seq would be exceeded */
-  PKV_ERR_DEVICE_TIMEOUT = -7  /* a kernel gave up waiting for a copy it issued (bounded wait) */
+  PKV_ERR_DEVICE_TIMEOUT = -7, /* a kernel gave up waiting for a copy it issued (bounded wait) */
+  PKV_ERR_SCRATCH_TOO_SMALL = -8 /* pkv_paged_decode_static: the call needs more than the built-in scratch */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -193,6 +194,30 @@ PKV_API pkv_status pkv_paged_decode(const pkv_pool* pool, float* out, const void
 /* Workspace bytes pkv_paged_decode needs for these arguments on the current device. */
 PKV_API size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t n_seqs, int32_t num_q_heads,
                                   int32_t partition_tokens);
+
+/* Paged decode for callers that may not allocate device memory at all.
+ *
+ * No counterpart on the source pages: this is a deployment convenience of this library. Some
+ * callers cannot call cudaMalloc or hand out scratch buffers: a plugin inside a host application
+ * that owns every device byte through its own fixed arena, a latency-critical serving loop where
+ * an allocation (and the device synchronisation it implies) is not acceptable, or a process with a
+ * memory budget fixed at start-up. This entry point takes the same arguments as pkv_paged_decode
+ * minus the workspace and instead uses a scratch array compiled into the library:
+ * PKV_STATIC_SCRATCH_BYTES (16 MiB) of device memory that every GPU which loads the library keeps
+ * until the process exits. It calls no allocator (no cudaMalloc, no cudaFree, no library routine
+ * that allocates).
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress with
+ *    that device current) and remembers it; make that first call before any stream capture.
+ *  - Every call on a device uses the same array. Its contents need no initialisation (each call
+ *    writes every scratch entry it later reads), but calls whose kernels overlap on the GPU (other
+ *    streams, other threads) race on it: serialise them, e.g. on one stream.
+ *  - A problem whose workspace (pkv_decode_workspace_bytes) exceeds PKV_STATIC_SCRATCH_BYTES is
+ *    rejected with PKV_ERR_SCRATCH_TOO_SMALL before anything is enqueued. */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
+PKV_API pkv_status pkv_paged_decode_static(const pkv_pool* pool, float* out, const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_tables,
+                                           const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads,
+                                           float scale, int32_t partition_tokens, void* stream);
 
 /* Synchronise the current device, then return and clear the error recorded by kernels
  * (PKV_ERR_DEVICE_BOUNDS / PKV_ERR_DEVICE_TIMEOUT), PKV_ERR_CUDA if the device reports an error,

@@ -32,6 +32,8 @@ lib = ctypes.CDLL(LIB_PATH)
 F32, BF16 = 0, 1
 OK, ERR_INVALID, ERR_NO_BLOCKS, ERR_NO_SEQ, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_CAPACITY, ERR_DEVICE_TIMEOUT = (
     0, -1, -2, -3, -4, -5, -6, -7)
+ERR_SCRATCH_TOO_SMALL = -8
+STATIC_SCRATCH_BYTES = 16 << 20
 
 _i32, _i64, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
 _pi32, _pi64 = ctypes.POINTER(_i32), ctypes.POINTER(_i64)
@@ -67,6 +69,8 @@ _SIGS = {
     "pkv_paged_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32, _vp,
                                         _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
+    "pkv_paged_decode_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32,
+                                               _vp]),
     "pkv_last_error": (ctypes.c_int, [_vp]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -263,6 +267,17 @@ class Pool:
         _check(lib.pkv_paged_decode(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache), _dev(block_tables),
                                     _dev(context_lens), n_seqs, num_q_heads, float(scale), int(partition_tokens),
                                     _dev(workspace), ws_bytes, _stream(stream)), "pkv_paged_decode")
+
+    def paged_decode_static(self, out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                            partition_tokens: int = 0, stream=None) -> None:
+        """pkv_paged_decode_static: like paged_decode, with the library's built-in scratch instead of a
+        caller workspace (for callers that must not allocate device memory). Calls that overlap on the
+        GPU share that scratch and race; keep them on one stream."""
+        n_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
+        _check(lib.pkv_paged_decode_static(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache),
+                                           _dev(block_tables), _dev(context_lens), n_seqs, num_q_heads,
+                                           float(scale), int(partition_tokens), _stream(stream)),
+               "pkv_paged_decode_static")
 
     def last_error(self) -> int:
         return lib.pkv_last_error(self._h)

@@ -97,6 +97,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_DEVICE_BOUNDS: return "kernel met a block id or slot outside the pool";
     case PKV_ERR_CAPACITY: return "sequence or block-table capacity exceeded";
     case PKV_ERR_DEVICE_TIMEOUT: return "kernel timed out waiting for its own copy";
+    case PKV_ERR_SCRATCH_TOO_SMALL: return "call needs more scratch than the library's built-in array holds";
   }
   return "unknown status";
 }

@@ -330,3 +330,48 @@ pkv_status pkv_last_error(const pkv_pool*) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// pkv_paged_decode_static: the same decode with scratch compiled into the library, for callers
+// that may not allocate device memory. The array below is part of the module image: each device
+// that loads the library holds it until the process exits. Host code must not use its name as an
+// address (on the host it is only a stand-in); the device address is looked up once per device.
+// ---------------------------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {};
+
+// Device address of g_static_scratch on the current device (looked up on first use per device).
+pkv_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) return PKV_ERR_CUDA;
+    g_static_ptr[dev] = ptr;
+  }
+  *out = g_static_ptr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_paged_decode_static(const pkv_pool* p, float* out, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads,
+                                              float scale, int32_t partition_tokens, void* stream) {
+  if (!p) return PKV_ERR_INVALID;
+  if (n_seqs == 0) return PKV_OK;
+  const size_t need = pkv_decode_workspace_bytes(p, n_seqs, num_q_heads, partition_tokens);
+  if (need == 0) return PKV_ERR_INVALID;
+  if (need > PKV_STATIC_SCRATCH_BYTES) return PKV_ERR_SCRATCH_TOO_SMALL;
+  void* scratch = nullptr;
+  const pkv_status st = static_scratch(&scratch);
+  if (st != PKV_OK) return st;
+  return pkv_paged_decode(p, out, q, k_cache, v_cache, block_tables, context_lens, n_seqs, num_q_heads, scale,
+                          partition_tokens, scratch, PKV_STATIC_SCRATCH_BYTES, stream);
+}
