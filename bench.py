@@ -318,7 +318,8 @@ def bench_cuda(args, world, rank, local):
             "bound": "hbm", "kernel": "paged_decode (decode + log-sum-exp reduce, one pkv_paged_decode call)",
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": None if traffic is None else traffic["bytes_per_launch_full"],
+            "traffic": None if traffic is None else int(traffic["bytes_per_launch_profile"] * dec_bytes_per_launch
+                                                         / traffic["algorithmic_bytes_profile"]),
             "algorithmic_bytes_per_launch": int(dec_bytes_per_launch),
             "mean_launch_us": round(1e3 * float(np.mean(dec_ms)), 2),
         },

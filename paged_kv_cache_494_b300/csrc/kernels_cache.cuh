@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
                                                                 int32_t Hkv, int32_t PPR, int32_t B, int64_t n_slots,
                                                                 uint4* __restrict__ k_cache,
                                                                 uint4* __restrict__ v_cache) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t total = static_cast<int64_t>(n_tokens) * Hkv * PPR;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
@@ -51,6 +53,8 @@ struct LayerCaches {
 // grid.x = n_pairs * num_layers; each CTA copies one K block and one V block (PPB pieces each).
 __global__ void __launch_bounds__(256) copy_blocks_kernel(LayerCaches caches, const int32_t* __restrict__ pairs,
                                                           int32_t num_layers, int64_t PPB, int32_t num_blocks) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int32_t pair = blockIdx.x / num_layers;
   const int32_t layer = blockIdx.x - pair * num_layers;
   const int32_t src = __ldg(pairs + 2 * pair);

@@ -119,48 +119,82 @@ __device__ __forceinline__ int64_t item_start(const int32_t* pref, const int32_t
 }
 
 // Shared-memory carve-up of the decode kernel: [1 KB alignment slack][ring: per warp `stages` stages]
-// [mbarriers][prefix arrays]. Stages start on 1024-byte boundaries (128-byte swizzle atoms).
+// [mbarriers][64-int scan scratch][prefix arrays]. Stages start on 1024-byte boundaries (128-byte
+// swizzle atoms).
 __host__ __device__ inline size_t decode_ring_bytes(int nw, int stages, int stage_bytes) {
   return static_cast<size_t>(nw) * stages * stage_bytes;
 }
 __host__ __device__ inline size_t decode_smem_bytes(int nw, int stages, int stage_bytes, int n_seqs) {
-  return 1024 + decode_ring_bytes(nw, stages, stage_bytes) + static_cast<size_t>(nw) * stages * 8 +
+  return 1024 + decode_ring_bytes(nw, stages, stage_bytes) + static_cast<size_t>(nw) * stages * 8 + 256 +
          2 * static_cast<size_t>(n_seqs + 1) * 4;
 }
 
-// Prefix sums over sequences of chunk counts (pref) and partition counts (ipref), by warp 0.
-__device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref, int32_t* ipref, int lane) {
+// Block-wide exclusive prefix sums over sequences of chunk counts (pref) and partition counts
+// (ipref); pref[n] / ipref[n] hold the totals. Every thread of the CTA takes part. Lengths are
+// loaded kPrefixBatch tiles at a time so that their latencies overlap. wsum: 64 ints of smem.
+constexpr int kPrefixBatch = 8;
+
+__device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref, int32_t* ipref, int32_t* wsum) {
   const int32_t n = a.n_seqs;
   const int32_t PC = a.part_chunks > 0 ? a.part_chunks : 1;
-  const int32_t per = (n + 31) / 32;
-  const int32_t lo = min(lane * per, n), hi = min(lo + per, n);
-  int32_t sc = 0, si = 0;
-  for (int32_t b = lo; b < hi; ++b) {
-    const int32_t nch = (clamped_len(a, b) + kChunk - 1) / kChunk;
-    sc += nch;
-    si += (nch + PC - 1) / PC;
-  }
-  int32_t ec = sc, ei = si;  // inclusive scan, then make exclusive
-  for (int off = 1; off < 32; off <<= 1) {
-    const int32_t tc = __shfl_up_sync(0xffffffffu, ec, off);
-    const int32_t ti = __shfl_up_sync(0xffffffffu, ei, off);
-    if (lane >= off) {
-      ec += tc;
-      ei += ti;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  const int32_t cap = a.MB * a.B;
+  int32_t carry_c = 0, carry_i = 0;  // running totals, identical in every thread
+  for (int32_t base = 0; base < n; base += nt * kPrefixBatch) {
+    int32_t raw[kPrefixBatch];
+#pragma unroll
+    for (int k = 0; k < kPrefixBatch; ++k) {
+      const int32_t b = base + k * nt + tid;
+      raw[k] = b < n ? __ldg(a.context_lens + b) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kPrefixBatch; ++k) {
+      if (base + k * nt >= n) break;  // uniform across the CTA
+      int32_t len = raw[k];
+      if (len < 0 || len > cap) {
+        record_error(ERRBIT_BOUNDS);
+        len = len < 0 ? 0 : cap;
+      }
+      const int32_t c = (len + kChunk - 1) / kChunk;
+      const int32_t ci = (c + PC - 1) / PC;
+      int32_t ic = c, ii = ci;  // inclusive warp scan
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t tc = __shfl_up_sync(0xffffffffu, ic, off);
+        const int32_t ti = __shfl_up_sync(0xffffffffu, ii, off);
+        if (lane >= off) {
+          ic += tc;
+          ii += ti;
+        }
+      }
+      if (lane == 31) {
+        wsum[warp] = ic;
+        wsum[32 + warp] = ii;
+      }
+      __syncthreads();
+      int32_t pc = 0, pi = 0, tc = 0, ti = 0;
+      for (int w2 = 0; w2 < nw; ++w2) {
+        const int32_t sc = wsum[w2], si = wsum[32 + w2];
+        if (w2 < warp) {
+          pc += sc;
+          pi += si;
+        }
+        tc += sc;
+        ti += si;
+      }
+      const int32_t b = base + k * nt + tid;
+      if (b < n) {
+        pref[b] = carry_c + pc + ic - c;
+        ipref[b] = carry_i + pi + ii - ci;
+      }
+      carry_c += tc;
+      carry_i += ti;
+      __syncthreads();  // wsum is reused by the next tile
     }
   }
-  ec -= sc;
-  ei -= si;
-  for (int32_t b = lo; b < hi; ++b) {
-    pref[b] = ec;
-    ipref[b] = ei;
-    const int32_t nch = (clamped_len(a, b) + kChunk - 1) / kChunk;
-    ec += nch;
-    ei += (nch + PC - 1) / PC;
-  }
-  if (lane == 31) {
-    pref[n] = ec;
-    ipref[n] = ei;
+  if (tid == 0) {
+    pref[n] = carry_c;
+    ipref[n] = carry_i;
   }
 }
 
@@ -488,10 +522,12 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   unsigned char* ring = smem + static_cast<size_t>(warp) * S * SB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + decode_ring_bytes(NW, S, SB)) + warp * S;
-  int32_t* pref = reinterpret_cast<int32_t*>(smem + decode_ring_bytes(NW, S, SB) + static_cast<size_t>(NW) * S * 8);
+  int32_t* wsum = reinterpret_cast<int32_t*>(smem + decode_ring_bytes(NW, S, SB) + static_cast<size_t>(NW) * S * 8);
+  int32_t* pref = wsum + 64;
   int32_t* ipref = pref + (n + 1);
 
-  if (warp == 0) build_prefix(a, pref, ipref, lane);
+  pdl_wait();
+  build_prefix(a, pref, ipref, wsum);
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
     fence_mbar_init();
@@ -504,7 +540,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
 
   // Empty sequences: zero rows (and mark their units complete for the reduce).
   for (int32_t b = w; b < n; b += W) {
-    if (clamped_len(a, b) != 0) continue;
+    if (pref[b + 1] != pref[b]) continue;
     float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(b) * a.Hq * D);
     for (int i = lane; i < a.Hq * D / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (PC == 0)
@@ -633,14 +669,23 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
     for (int64_t k = i + 1; k < issued; ++k)
       mbar_wait_bounded(smem_addr(bars + static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1));
   }
+  pdl_launch_dependents();
 }
 
 // ------------------------------------------------------------------------------------------------
-// Log-sum-exp merge of the segments of split units. One CTA per unit (b, h).
+// Log-sum-exp merge of the segments of split units: one warp per unit (b, h), 8 warps per CTA.
+// Online form over the segments (running max M, weight sum, accumulator), so every segment's
+// loads are independent of the previous segment's arithmetic and can be in flight together.
 // ------------------------------------------------------------------------------------------------
+constexpr int kReduceWarps = 8;
+
 template <int D, int G>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(DecodeArgs a) {
-  const int64_t u = blockIdx.x;
+__global__ void __launch_bounds__(32 * kReduceWarps) decode_reduce_kernel(const __grid_constant__ DecodeArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t u = static_cast<int64_t>(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5);
+  if (u >= static_cast<int64_t>(a.n_seqs) * a.Hkv) return;
   const int32_t b = static_cast<int32_t>(u / a.Hkv);
   const int32_t h = static_cast<int32_t>(u - static_cast<int64_t>(b) * a.Hkv);
   int64_t first_slot, n_parts;
@@ -652,7 +697,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(DecodeArgs a) {
     first_kind = d0 & 1;
     const int32_t w_last = a.ws_desc[2 * u + 1];
     if (w_last < first_slot || w_last >= a.total_warps) {   // never written by a finished decode
-      if (threadIdx.x == 0) record_error(ERRBIT_BOUNDS);
+      if (lane == 0) record_error(ERRBIT_BOUNDS);
       return;
     }
     n_parts = w_last - first_slot + 1;
@@ -661,31 +706,31 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(DecodeArgs a) {
     n_parts = (nch + a.part_chunks - 1) / a.part_chunks;
     if (n_parts <= 1) return;
     if (n_parts > a.max_parts) {
-      if (threadIdx.x == 0) record_error(ERRBIT_BOUNDS);
+      if (lane == 0) record_error(ERRBIT_BOUNDS);
       return;
     }
     first_slot = u * a.max_parts;
   }
-  auto slot_of = [&](int64_t k) -> int64_t {
-    if (a.part_chunks != 0) return first_slot + k;
-    return 2 * (first_slot + k) + (k == 0 ? first_kind : 0);
-  };
-  for (int idx = threadIdx.x; idx < G * D / 4; idx += blockDim.x) {
+  constexpr int V4 = G * D / 4;  // float4 values per unit
+  for (int idx = lane; idx < V4; idx += 32) {
     const int j = idx / (D / 4);
     const int d4 = idx - j * (D / 4);
-    float M = -INFINITY;
-    for (int64_t k = 0; k < n_parts; ++k) M = fmaxf(M, a.ws_ml[(slot_of(k) * G + j) * 2]);
-    float wsum = 0.f;
+    float M = -INFINITY, wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int64_t k = 0; k < n_parts; ++k) {
-      const int64_t s = slot_of(k);
-      const float wk = a.ws_ml[(s * G + j) * 2 + 1] * exp2f(a.ws_ml[(s * G + j) * 2] - M);
+      const int64_t s = (a.part_chunks != 0) ? first_slot + k : 2 * (first_slot + k) + (k == 0 ? first_kind : 0);
+      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2);
       const float4 o = reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D)[d4];
-      acc.x = fmaf(wk, o.x, acc.x);
-      acc.y = fmaf(wk, o.y, acc.y);
-      acc.z = fmaf(wk, o.z, acc.z);
-      acc.w = fmaf(wk, o.w, acc.w);
-      wsum += wk;
+      const float Mn = fmaxf(M, ml.x);
+      const float c = exp2f(M - Mn);         // rescales what was accumulated so far (0 at the start)
+      const float wk = ml.y * exp2f(ml.x - Mn);
+      acc.x = fmaf(wk, o.x, acc.x * c);
+      acc.y = fmaf(wk, o.y, acc.y * c);
+      acc.z = fmaf(wk, o.z, acc.z * c);
+      acc.w = fmaf(wk, o.w, acc.w * c);
+      wsum = fmaf(wsum, c, wk);
+      M = Mn;
     }
     const float inv = 1.f / wsum;
     reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[d4] =

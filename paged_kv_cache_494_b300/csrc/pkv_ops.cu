@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "kernels_cache.cuh"
 #include "kernels_decode.cuh"
@@ -33,6 +34,33 @@ int num_sms() {
   if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   cached[dev].store(v, std::memory_order_relaxed);
   return v;
+}
+
+// Programmatic dependent launch on every libpagedkv kernel unless PKV_PDL=0. Each kernel waits for
+// its predecessor in the stream (griddepcontrol.wait) before touching global memory, so only the
+// launch latency overlaps; data ordering is plain stream order.
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* s = std::getenv("PKV_PDL");
+    return !(s && std::strcmp(s, "0") == 0);
+  }();
+  return on;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 int env_int(const char* name, int fallback) {
@@ -225,11 +253,12 @@ pkv_status pkv_reshape_and_cache(const pkv_pool* p, const void* k, const void* v
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int grid = static_cast<int>(want < 65535 * 4 ? want : 65535 * 4);
-  pkv_dev::reshape_and_cache_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, n_tokens, d.num_kv_heads, ppr,
-      d.block_size, static_cast<int64_t>(d.num_blocks) * d.block_size, static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache));
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const cudaError_t e = launch(pkv_dev::reshape_and_cache_kernel, dim3(grid), dim3(threads), 0,
+                               static_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
+                               static_cast<const uint4*>(v), slots, n_tokens, d.num_kv_heads, ppr, d.block_size,
+                               static_cast<int64_t>(d.num_blocks) * d.block_size, static_cast<uint4*>(k_cache),
+                               static_cast<uint4*>(v_cache));
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status pkv_copy_blocks(const pkv_pool* p, void* const* k_caches, void* const* v_caches, const int32_t* pairs,
@@ -251,9 +280,10 @@ pkv_status pkv_copy_blocks(const pkv_pool* p, void* const* k_caches, void* const
   if (block_bytes % 16 != 0) return PKV_ERR_INVALID;
   const int64_t grid = static_cast<int64_t>(n_pairs) * d.num_layers;
   if (grid > 0x7fffffff) return PKV_ERR_INVALID;
-  pkv_dev::copy_blocks_kernel<<<static_cast<unsigned>(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      lc, pairs, d.num_layers, block_bytes / 16, d.num_blocks);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const cudaError_t e = launch(pkv_dev::copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                               static_cast<cudaStream_t>(stream), lc, pairs, d.num_layers, block_bytes / 16,
+                               d.num_blocks);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? PKV_OK : PKV_ERR_CUDA;
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_pool* p, int32_t n_seqs, int32_t num_q_heads, int32_t partition_tokens) {
@@ -310,12 +340,16 @@ pkv_status pkv_paged_decode(const pkv_pool* p, float* out, const void* q, const 
     if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d)) return PKV_ERR_CUDA;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  pl.k.decode<<<pl.grid, pl.nw * 32, pl.smem, s>>>(a, maps);
-  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-  const int64_t units = pl.n_units;
-  if (units > 0x7fffffff) return PKV_ERR_INVALID;
-  pl.k.reduce<<<static_cast<unsigned>(units), 128, 0, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  const int64_t reduce_ctas = (pl.n_units + pkv_dev::kReduceWarps - 1) / pkv_dev::kReduceWarps;
+  if (reduce_ctas > 0x7fffffff) return PKV_ERR_INVALID;
+  if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (launch(pl.k.reduce, dim3(static_cast<unsigned>(reduce_ctas)), dim3(32 * pkv_dev::kReduceWarps), 0, s, a) !=
+          cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 pkv_status pkv_last_error(const pkv_pool*) {
