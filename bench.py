@@ -250,8 +250,8 @@ def bench_cuda(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     dist = init_dist(world, "nccl")
-    steps_total = args.warmup + args.steps
-    s = Serve(args.seed + rank, 2 * steps_total + 2, device)
+    steps_total = args.warmup + 2 * args.steps
+    s = Serve(args.seed + rank, 2 * steps_total + args.warmup + args.steps + 4, device)
     pkv = s.pkv
     plan = s.plan_steps(steps_total)
     Ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -261,7 +261,7 @@ def bench_cuda(args, world, rank, local):
     torch.cuda.synchronize()
     assert pkv.last_error() == pkv.OK
 
-    dec_events = [[[Ev(), Ev()] for _ in range(s.L)] for _ in range(args.steps)]
+    # timed region 1 (`value`): K steps exactly as a user would enqueue them, nothing else inside
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -270,7 +270,7 @@ def bench_cuda(args, world, rank, local):
     with ClockSampler(local) as clocks:
         start.record(s.stream)
         for k in range(args.steps):
-            launches += s.run_step(plan[args.warmup + k], dec_events[k])
+            launches += s.run_step(plan[args.warmup + k])
         stop.record(s.stream)
         torch.cuda.synchronize()
     if dist is not None:
@@ -282,8 +282,18 @@ def bench_cuda(args, world, rank, local):
     kv_bytes_all = sum_over_ranks(kv_bytes, dist, device)
     seq_steps_all = sum_over_ranks(s.n * args.steps, dist, device)
     value = kv_bytes_all / (t_ms_max * 1e-3) / 1e9
+
+    # timed region 2 (roofline): the next K steps with CUDA events around every decode call on the
+    # launch stream (the events cut the programmatic launch overlap, so this pass is kept separate)
+    dec_events = [[[Ev(), Ev()] for _ in range(s.L)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        s.run_step(plan[args.warmup + args.steps + k], dec_events[k])
+    torch.cuda.synchronize()
+    assert pkv.last_error() == pkv.OK
     dec_ms = [dec_events[k][l][0].elapsed_time(dec_events[k][l][1]) for k in range(args.steps) for l in range(s.L)]
-    dec_bytes_per_launch = kv_bytes / (args.steps * s.L)
+    dec_bytes = sum(s.kv_bytes(plan[args.warmup + args.steps + k][3]) for k in range(args.steps))
+    dec_bytes_per_launch = dec_bytes / (args.steps * s.L)
     achieved = dec_bytes_per_launch / (float(np.mean(dec_ms)) * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
 
@@ -337,8 +347,12 @@ def bench_cuda(args, world, rank, local):
 
 
 def bench_e2e(s: Serve, args, dist, device):
-    """Same metric through the public API with host buffers: allocator call, H2D of the step's
-    inputs from pinned memory, the kernels, and D2H of every layer's output, all timed."""
+    """Same metric through the public API with host buffers, all inside the timed region: the host
+    allocator call (pkv_append), host->device copies of the step's inputs from pinned memory (slots,
+    block tables, lengths, and q / k / v of every layer), the kernels, and the device->host copy of
+    every layer's output. Copies run on their own streams so that layer l's inputs upload while
+    layer l-1 computes and layer l-2's output downloads; device and pinned staging buffers are
+    double-buffered across steps (a step reuses the buffers of the step before last)."""
     torch = s.torch
     L, n = s.L, s.n
     pin = lambda t: t.cpu().pin_memory()
@@ -346,40 +360,55 @@ def bench_e2e(s: Serve, args, dist, device):
     hk = [pin(t) for t in s.k_new]
     hv = [pin(t) for t in s.v_new]
     hout = [torch.empty(n, s.Hq, s.D, dtype=torch.float32).pin_memory() for _ in range(L)]
-    dq = [torch.empty_like(t) for t in s.q]
-    dk = [torch.empty_like(t) for t in s.k_new]
-    dv = [torch.empty_like(t) for t in s.v_new]
-    h_slots = torch.empty(n, dtype=torch.int64).pin_memory()
-    h_tab = torch.empty(n, s.MB, dtype=torch.int32).pin_memory()
-    h_len = torch.empty(n, dtype=torch.int32).pin_memory()
-    d_slots = torch.empty(n, dtype=torch.int64, device=device)
-    d_tab = torch.empty(n, s.MB, dtype=torch.int32, device=device)
-    d_len = torch.empty(n, dtype=torch.int32, device=device)
-    st = s.stream
-    done = torch.cuda.Event()
+    dq = [[torch.empty_like(t) for t in s.q] for _ in range(2)]
+    dk = [[torch.empty_like(t) for t in s.k_new] for _ in range(2)]
+    dv = [[torch.empty_like(t) for t in s.v_new] for _ in range(2)]
+    dout = [[torch.empty_like(t) for t in s.out] for _ in range(2)]
+    h_slots = [torch.empty(n, dtype=torch.int64).pin_memory() for _ in range(2)]
+    h_tab = [torch.empty(n, s.MB, dtype=torch.int32).pin_memory() for _ in range(2)]
+    h_len = [torch.empty(n, dtype=torch.int32).pin_memory() for _ in range(2)]
+    d_slots = [torch.empty(n, dtype=torch.int64, device=device) for _ in range(2)]
+    d_tab = [torch.empty(n, s.MB, dtype=torch.int32, device=device) for _ in range(2)]
+    d_len = [torch.empty(n, dtype=torch.int32, device=device) for _ in range(2)]
+    s_h2d, s_comp, s_d2h = torch.cuda.Stream(device), torch.cuda.Stream(device), torch.cuda.Stream(device)
+    step_done = [torch.cuda.Event(), torch.cuda.Event()]
+    for e in step_done:
+        e.record(s_d2h)
+    ev_in = [[torch.cuda.Event() for _ in range(L)] for _ in range(2)]
+    ev_out = [[torch.cuda.Event() for _ in range(L)] for _ in range(2)]
+    count = [0]
 
     def step():
-        done.synchronize()            # pinned staging buffers are reused: previous step must be done
+        p = count[0] & 1
+        count[0] += 1
+        step_done[p].synchronize()    # the step before last has released parity p's buffers
         slots, pairs = s.pool.append(s.seqs)
         tables, lens = s.pool.block_table(s.seqs)
-        h_slots.numpy()[:] = slots
-        h_tab.numpy()[:] = tables
-        h_len.numpy()[:] = lens
-        d_slots.copy_(h_slots, non_blocking=True)
-        d_tab.copy_(h_tab, non_blocking=True)
-        d_len.copy_(h_len, non_blocking=True)
+        h_slots[p].numpy()[:] = slots
+        h_tab[p].numpy()[:] = tables
+        h_len[p].numpy()[:] = lens
+        with torch.cuda.stream(s_h2d):
+            d_slots[p].copy_(h_slots[p], non_blocking=True)
+            d_tab[p].copy_(h_tab[p], non_blocking=True)
+            d_len[p].copy_(h_len[p], non_blocking=True)
+            for l in range(L):
+                dq[p][l].copy_(hq[l], non_blocking=True)
+                dk[p][l].copy_(hk[l], non_blocking=True)
+                dv[p][l].copy_(hv[l], non_blocking=True)
+                ev_in[p][l].record(s_h2d)
         for l in range(L):
-            dq[l].copy_(hq[l], non_blocking=True)
-            dk[l].copy_(hk[l], non_blocking=True)
-            dv[l].copy_(hv[l], non_blocking=True)
-            s.pool.reshape_and_cache(dk[l], dv[l], d_slots, s.k_caches[l], s.v_caches[l], stream=st)
-            s.pool.paged_decode(s.out[l], dq[l], s.k_caches[l], s.v_caches[l], d_tab, d_len, s.w.scale, 0, s.ws,
-                                stream=st)
-            hout[l].copy_(s.out[l], non_blocking=True)
-        done.record(st)
+            s_comp.wait_event(ev_in[p][l])
+            s.pool.reshape_and_cache(dk[p][l], dv[p][l], d_slots[p], s.k_caches[l], s.v_caches[l], stream=s_comp)
+            s.pool.paged_decode(dout[p][l], dq[p][l], s.k_caches[l], s.v_caches[l], d_tab[p], d_len[p], s.w.scale,
+                                0, s.ws, stream=s_comp)
+            ev_out[p][l].record(s_comp)
+        with torch.cuda.stream(s_d2h):
+            for l in range(L):
+                s_d2h.wait_event(ev_out[p][l])
+                hout[l].copy_(dout[p][l], non_blocking=True)
+            step_done[p].record(s_d2h)
         return lens.astype(np.int64)
 
-    done.record(st)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -397,7 +426,8 @@ def bench_e2e(s: Serve, args, dist, device):
     d2h = L * hout[0].numel() * 4
     assert s.pkv.last_error() == s.pkv.OK
     return {"value": round(kv_all / t_max / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(1e3 * t_max / args.steps, 3)}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(1e3 * t_max / args.steps, 3),
+            "timing": "wall clock (perf_counter) around K steps, device synchronised at both ends"}
 
 
 # ------------------------------------------------------------------------------------------------

@@ -711,30 +711,54 @@ __global__ void __launch_bounds__(32 * kReduceWarps) decode_reduce_kernel(const 
     }
     first_slot = u * a.max_parts;
   }
-  constexpr int V4 = G * D / 4;  // float4 values per unit
-  for (int idx = lane; idx < V4; idx += 32) {
-    const int j = idx / (D / 4);
-    const int d4 = idx - j * (D / 4);
-    float M = -INFINITY, wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int64_t k = 0; k < n_parts; ++k) {
-      const int64_t s = (a.part_chunks != 0) ? first_slot + k : 2 * (first_slot + k) + (k == 0 ? first_kind : 0);
-      const float2 ml = *reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2);
-      const float4 o = reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D)[d4];
-      const float Mn = fmaxf(M, ml.x);
-      const float c = exp2f(M - Mn);         // rescales what was accumulated so far (0 at the start)
-      const float wk = ml.y * exp2f(ml.x - Mn);
-      acc.x = fmaf(wk, o.x, acc.x * c);
-      acc.y = fmaf(wk, o.y, acc.y * c);
-      acc.z = fmaf(wk, o.z, acc.z * c);
-      acc.w = fmaf(wk, o.w, acc.w * c);
-      wsum = fmaf(wsum, c, wk);
-      M = Mn;
+  constexpr int V4 = G * D / 4;          // float4 values per unit
+  constexpr int R = (V4 + 31) / 32;       // per lane
+  float M[R], wsum[R];
+  float4 acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    M[r] = -INFINITY;
+    wsum[r] = 0.f;
+    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll 2
+  for (int64_t k = 0; k < n_parts; ++k) {
+    const int64_t s = (a.part_chunks != 0) ? first_slot + k : 2 * (first_slot + k) + (k == 0 ? first_kind : 0);
+    float2 ml[R];
+    float4 o[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {      // all of this segment's loads first
+      const int idx = lane + 32 * r;
+      if (idx < V4) {
+        const int j = idx / (D / 4);
+        ml[r] = *reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2);
+        o[r] = reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D)[idx - j * (D / 4)];
+      }
     }
-    const float inv = 1.f / wsum;
-    reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[d4] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (lane + 32 * r < V4) {
+        const float Mn = fmaxf(M[r], ml[r].x);
+        const float c = exp2f(M[r] - Mn);  // rescales what was accumulated so far (0 at the start)
+        const float wk = ml[r].y * exp2f(ml[r].x - Mn);
+        acc[r].x = fmaf(wk, o[r].x, acc[r].x * c);
+        acc[r].y = fmaf(wk, o[r].y, acc[r].y * c);
+        acc[r].z = fmaf(wk, o[r].z, acc[r].z * c);
+        acc[r].w = fmaf(wk, o[r].w, acc[r].w * c);
+        wsum[r] = fmaf(wsum[r], c, wk);
+        M[r] = Mn;
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int idx = lane + 32 * r;
+    if (idx < V4) {
+      const int j = idx / (D / 4);
+      const float inv = 1.f / wsum[r];
+      reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[idx - j * (D / 4)] =
+          make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
+    }
   }
 }
 
