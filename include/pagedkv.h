@@ -142,6 +142,15 @@ PKV_API pkv_status pkv_fork(pkv_pool* pool, int32_t parent, int32_t* child_out);
  * reaches zero goes on top of the free list. Blocks still referenced elsewhere stay in use. */
 PKV_API pkv_status pkv_free(pkv_pool* pool, int32_t seq);
 
+/* Sliding-window release: drop this sequence's reference to every block whose positions all lie
+ * before `position` (0 <= position <= length), in table order; a block reaching refcount 0 goes on
+ * top of the free list. Released table entries become -1 (a hole); the sequence length is unchanged,
+ * so later appends and the slots of remaining positions do not move. Decode with a window that starts
+ * at or after `position` never reads the holes ("Adaptar el presupuesto a la estrategia de caché":
+ * a window bounds the history a sequence keeps). *n_released_out (may be NULL) = references dropped.
+ * Errors: NO_SEQ, INVALID (position out of range). */
+PKV_API pkv_status pkv_release_before(pkv_pool* pool, int32_t seq, int32_t position, int32_t* n_released_out);
+
 /* Host copies of the block tables of n live sequences: table_out[n][max_blocks_per_seq]
  * (int32, unused entries -1) and lens_out[n]. Either output may be NULL. */
 PKV_API pkv_status pkv_block_table(const pkv_pool* pool, const int32_t* seqs, int32_t n, int32_t* table_out,
@@ -190,6 +199,18 @@ PKV_API pkv_status pkv_paged_decode(const pkv_pool* pool, float* out, const void
                             const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                             int32_t n_seqs, int32_t num_q_heads, float scale, int32_t partition_tokens,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* Sliding-window variant: as pkv_paged_decode, but each query attends only to the last `window`
+ * positions of its sequence, t in [max(0, len_b - window), len_b) ("¿Cuánta memoria reservar para la
+ * caché KV?", "Adaptar el presupuesto a la estrategia de caché": a sliding-window layer keeps a
+ * bounded history). window = 0 means no window (identical to pkv_paged_decode). Blocks entirely
+ * before the window are never read, so they may have been released with pkv_release_before (their
+ * table entries are then -1). Uses the same workspace size as pkv_paged_decode. */
+PKV_API pkv_status pkv_paged_decode_window(const pkv_pool* pool, float* out, const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_tables,
+                                           const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads,
+                                           float scale, int32_t window, int32_t partition_tokens, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /* Workspace bytes pkv_paged_decode needs for these arguments on the current device. */
 PKV_API size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t n_seqs, int32_t num_q_heads,

@@ -165,14 +165,42 @@ class PoolModel:
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
         for b in self.tables[child]:
-            self.refcount[b] += 1
+            if b >= 0:
+                self.refcount[b] += 1
         return OK, child
+
+    def release_before(self, seq: int, position: int) -> Tuple[int, int]:
+        """Drop the sequence's reference to every block whose positions all lie before ``position``.
+
+        Reading of the pages ("¿Cuánta memoria reservar para la caché KV?", "Adaptar el presupuesto a
+        la estrategia de caché": a sliding window bounds the history a sequence keeps): those blocks
+        are no longer attended to, so they are released in table order and their entries become -1;
+        the length (and every remaining slot) is unchanged. Returns (status, references dropped)."""
+        if seq not in self.tables:
+            return ERR_NO_SEQ, 0
+        if position < 0 or position > self.lens[seq]:
+            return ERR_INVALID, 0
+        t = self.tables[seq]
+        released = 0
+        for i in range(len(t)):
+            if (i + 1) * self.B > position:
+                break
+            if t[i] < 0:
+                continue
+            self.refcount[t[i]] -= 1
+            if self.refcount[t[i]] == 0:
+                self.free.append(t[i])
+            t[i] = -1
+            released += 1
+        return OK, released
 
     def free_seq(self, seq: int) -> int:
         """Drop one reference to every block of ``seq`` in table order; a block at zero is freed."""
         if seq not in self.tables:
             return ERR_NO_SEQ
         for b in self.tables.pop(seq):
+            if b < 0:
+                continue
             self.refcount[b] -= 1
             if self.refcount[b] == 0:
                 self.free.append(b)

@@ -46,7 +46,8 @@ def gather_sequence(cache: np.ndarray, table: Sequence[int], length: int, kv_hea
     Logical position t lives in physical block table[t // B] at offset t % B.
     """
     B = cache.shape[2]
-    rows = [cache[int(table[t // B]), kv_head, t % B, :] for t in range(length)]
+    rows = [cache[int(table[t // B]), kv_head, t % B, :] if int(table[t // B]) >= 0
+            else np.full(cache.shape[3], np.nan, dtype=cache.dtype) for t in range(length)]
     if not rows:
         return np.zeros((0, cache.shape[3]), dtype=np.float64)
     return to_f64(np.stack(rows))
@@ -59,11 +60,21 @@ def dense_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -
     return (p @ V) / p.sum()
 
 
+def window_start(length: int, window: int) -> int:
+    """First attended position under a sliding window (0 when window == 0 means no window).
+
+    Reading of "¿Cuánta memoria reservar para la caché KV?", "Adaptar el presupuesto a la estrategia
+    de caché": a sliding-window layer keeps only its most recent positions; here the last ``window``.
+    """
+    return max(0, length - window) if window > 0 else 0
+
+
 def paged_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables: np.ndarray,
-                 lens: Sequence[int], scale: float) -> np.ndarray:
+                 lens: Sequence[int], scale: float, window: int = 0) -> np.ndarray:
     """Decode attention for every (sequence, query head): out[b, j] in binary64.
 
     q: [n_seqs, Hq, D] stored values; caches: [NB, Hkv, B, D]; tables: [n_seqs, MB] int.
+    With window > 0 only positions [max(0, len - window), len) are attended to.
     """
     n, Hq, D = q.shape
     Hkv = k_cache.shape[1]
@@ -74,9 +85,10 @@ def paged_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables
         L = int(lens[b])
         if L == 0:
             continue
+        t0 = window_start(L, window)
         for h in range(Hkv):
-            K = gather_sequence(k_cache, tables[b], L, h)
-            V = gather_sequence(v_cache, tables[b], L, h)
+            K = gather_sequence(k_cache, tables[b], L, h)[t0:]
+            V = gather_sequence(v_cache, tables[b], L, h)[t0:]
             for j in range(h * g, (h + 1) * g):
                 out[b, j] = dense_attention(qd[b, j], K, V, scale)
     return out

@@ -13,6 +13,9 @@
  * GQA ("¿Cuánta memoria reservar para la caché KV?", "Emplear las cabezas KV"): query
  * head j reads KV head j / (Hq / Hkv).
  *
+ * Sliding window ("¿Cuánta memoria reservar para la caché KV?", "Adaptar el presupuesto a la
+ * estrategia de caché"): with window > 0 only positions [max(0, len - window), len) are attended to.
+ *
  * Storage types: 0 = float32, 1 = bfloat16 bit patterns (decoded exactly).
  * Cache layout: cache[block][kv_head][offset][dim].
  */
@@ -34,7 +37,7 @@ static double load_value(const void* base, int dtype, size_t idx) {
  * Returns the number of OpenMP threads used, or -1 on invalid arguments. */
 int oracle_decode(double* out, const void* q, int q_dtype, const void* k_cache, const void* v_cache,
                   int kv_dtype, const int32_t* tables, const int32_t* lens, int n_seqs, int num_q_heads,
-                  int num_kv_heads, int head_dim, int block_size, int max_blocks, double scale,
+                  int num_kv_heads, int head_dim, int block_size, int max_blocks, double scale, int window,
                   const int32_t* rows, int n_rows, int n_threads) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0) return -1;
   const int g = num_q_heads / num_kv_heads;
@@ -52,18 +55,21 @@ int oracle_decode(double* out, const void* q, int q_dtype, const void* k_cache, 
       const int b = (int)(flat / num_q_heads);
       const int j = (int)(flat % num_q_heads);
       const int h = j / g;
-      const int L = lens[b];
+      const int len = lens[b];
       double* o = out + r * D;
       for (int d = 0; d < D; ++d) o[d] = 0.0;
-      if (L <= 0) continue;
+      if (len <= 0) continue;
+      const int t0 = (window > 0 && len > window) ? len - window : 0;   /* first attended position */
+      const int L = len - t0;
       double* K = (double*)malloc(sizeof(double) * (size_t)L * D);
       double* V = (double*)malloc(sizeof(double) * (size_t)L * D);
       double* s = (double*)malloc(sizeof(double) * (size_t)L);
       double* qv = (double*)malloc(sizeof(double) * (size_t)D);
       /* rebuild the contiguous sequence through the block table */
       for (int t = 0; t < L; ++t) {
-        const long blk = tables[(long)b * max_blocks + t / block_size];
-        const size_t base = (((size_t)blk * num_kv_heads + h) * block_size + (t % block_size)) * D;
+        const int pos = t0 + t;
+        const long blk = tables[(long)b * max_blocks + pos / block_size];
+        const size_t base = (((size_t)blk * num_kv_heads + h) * block_size + (pos % block_size)) * D;
         for (int d = 0; d < D; ++d) {
           K[(size_t)t * D + d] = load_value(k_cache, kv_dtype, base + d);
           V[(size_t)t * D + d] = load_value(v_cache, kv_dtype, base + d);

@@ -36,7 +36,7 @@ def _load():
         f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
-                      ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+                      ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     return _lib
 
 
@@ -50,8 +50,9 @@ def _dtype_code(a: np.ndarray) -> int:
 
 def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables: np.ndarray,
            lens: np.ndarray, scale: float, rows: Optional[Sequence[int]] = None,
-           n_threads: int = 0, return_threads: bool = False):
+           n_threads: int = 0, return_threads: bool = False, window: int = 0):
     """Binary64 paged decode. q [n, Hq, D]; caches [NB, Hkv, B, D]; tables [n, MB].
+    window > 0: attend only to the last ``window`` positions of each sequence.
 
     Returns out [n, Hq, D] (rows=None) or [len(rows), D] for flat (b * Hq + j) ids.
     """
@@ -69,7 +70,7 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables: np.n
     out = np.zeros((n_rows, D), dtype=np.float64)
     used = lib.oracle_decode(out.ctypes.data, q.ctypes.data, _dtype_code(q), k_cache.ctypes.data,
                              v_cache.ctypes.data, _dtype_code(k_cache), tables.ctypes.data, lens.ctypes.data,
-                             n, Hq, Hkv, D, B, tables.shape[1], float(scale),
+                             n, Hq, Hkv, D, B, tables.shape[1], float(scale), int(window),
                              None if rows_arr is None else rows_arr.ctypes.data, n_rows, int(n_threads))
     if used < 0:
         raise ValueError("oracle_decode rejected its arguments")
@@ -84,7 +85,7 @@ def decode_fn_from(lib_path: str):
     f.restype = ctypes.c_int
     f.argtypes = _load().oracle_decode.argtypes
 
-    def run(q, k_cache, v_cache, tables, lens, scale):
+    def run(q, k_cache, v_cache, tables, lens, scale, window=0):
         q = np.ascontiguousarray(q)
         k_cache = np.ascontiguousarray(k_cache)
         v_cache = np.ascontiguousarray(v_cache)
@@ -95,6 +96,6 @@ def decode_fn_from(lib_path: str):
         out = np.zeros((n * Hq, D), dtype=np.float64)
         f(out.ctypes.data, q.ctypes.data, _dtype_code(q), k_cache.ctypes.data, v_cache.ctypes.data,
           _dtype_code(k_cache), tables.ctypes.data, lens.ctypes.data, n, Hq, Hkv, D, B, tables.shape[1],
-          float(scale), None, n * Hq, 1)
+          float(scale), int(window), None, n * Hq, 1)
         return out.reshape(n, Hq, D)
     return run

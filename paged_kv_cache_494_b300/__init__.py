@@ -62,12 +62,15 @@ _SIGS = {
     "pkv_fork": (ctypes.c_int, [_vp, _i32, _pi32]),
     "pkv_free": (ctypes.c_int, [_vp, _i32]),
     "pkv_block_table": (ctypes.c_int, [_vp, _pi32, _i32, _pi32, _pi32]),
+    "pkv_release_before": (ctypes.c_int, [_vp, _i32, _i32, _pi32]),
     "pkv_pool_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
     "pkv_export_state": (ctypes.c_int, [_vp, _pi32, _pi32, _pi32]),
     "pkv_reshape_and_cache": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp]),
     "pkv_copy_blocks": (ctypes.c_int, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _i32, _vp]),
     "pkv_paged_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32, _vp,
                                         _sz, _vp]),
+    "pkv_paged_decode_window": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
+                                               _i32, _i32, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
     "pkv_paged_decode_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32,
                                                _vp]),
@@ -223,6 +226,17 @@ class Pool:
     def free(self, seq: int) -> None:
         _check(self.free_raw(seq), "pkv_free")
 
+    def release_before_raw(self, seq: int, position: int) -> Tuple[int, int]:
+        n = _i32(0)
+        st = lib.pkv_release_before(self._h, int(seq), int(position), ctypes.byref(n))
+        return st, n.value
+
+    def release_before(self, seq: int, position: int) -> int:
+        """Sliding window: release the blocks of ``seq`` that lie entirely before ``position``."""
+        st, n = self.release_before_raw(seq, position)
+        _check(st, "pkv_release_before")
+        return n
+
     def block_table(self, seqs: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
         s = np.ascontiguousarray(list(seqs), dtype=np.int32)
         tables = np.zeros((max(s.size, 1), self.max_blocks_per_seq), dtype=np.int32)
@@ -261,9 +275,16 @@ class Pool:
         return int(lib.pkv_decode_workspace_bytes(self._h, int(n_seqs), int(num_q_heads), int(partition_tokens)))
 
     def paged_decode(self, out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                     partition_tokens: int = 0, workspace=None, stream=None) -> None:
+                     partition_tokens: int = 0, workspace=None, stream=None, window: int = 0) -> None:
+        """pkv_paged_decode, or pkv_paged_decode_window when window > 0."""
         n_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
         ws_bytes = 0 if workspace is None else int(workspace.numel() * workspace.element_size())
+        if window > 0:
+            _check(lib.pkv_paged_decode_window(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache),
+                                               _dev(block_tables), _dev(context_lens), n_seqs, num_q_heads,
+                                               float(scale), int(window), int(partition_tokens), _dev(workspace),
+                                               ws_bytes, _stream(stream)), "pkv_paged_decode_window")
+            return
         _check(lib.pkv_paged_decode(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache), _dev(block_tables),
                                     _dev(context_lens), n_seqs, num_q_heads, float(scale), int(partition_tokens),
                                     _dev(workspace), ws_bytes, _stream(stream)), "pkv_paged_decode")

@@ -56,6 +56,7 @@ struct DecodeArgs {
   int32_t max_parts;             // fixed mode: partition slots per unit
   int32_t stages;                // ring depth per warp
   int32_t total_warps;           // warps of the decode grid (balanced-mode slot count / 2)
+  int32_t window;                // > 0: attend only to the last `window` positions (sliding window)
   float scale_log2;              // scale * log2(e)
 };
 
@@ -119,22 +120,25 @@ __device__ __forceinline__ int64_t item_start(const int32_t* pref, const int32_t
 }
 
 // Shared-memory carve-up of the decode kernel: [1 KB alignment slack][ring: per warp `stages` stages]
-// [mbarriers][64-int scan scratch][prefix arrays]. Stages start on 1024-byte boundaries (128-byte
-// swizzle atoms).
+// [mbarriers][64-int scan scratch][pref][ipref][cfirst]. Stages start on 1024-byte boundaries
+// (128-byte swizzle atoms).
 __host__ __device__ inline size_t decode_ring_bytes(int nw, int stages, int stage_bytes) {
   return static_cast<size_t>(nw) * stages * stage_bytes;
 }
 __host__ __device__ inline size_t decode_smem_bytes(int nw, int stages, int stage_bytes, int n_seqs) {
   return 1024 + decode_ring_bytes(nw, stages, stage_bytes) + static_cast<size_t>(nw) * stages * 8 + 256 +
-         2 * static_cast<size_t>(n_seqs + 1) * 4;
+         3 * static_cast<size_t>(n_seqs + 1) * 4;
 }
 
 // Block-wide exclusive prefix sums over sequences of chunk counts (pref) and partition counts
-// (ipref); pref[n] / ipref[n] hold the totals. Every thread of the CTA takes part. Lengths are
-// loaded kPrefixBatch tiles at a time so that their latencies overlap. wsum: 64 ints of smem.
+// (ipref); pref[n] / ipref[n] hold the totals; cfirst[b] is the first chunk of sequence b that
+// the attention reads (0, or the chunk holding position len - window). Every thread of the CTA
+// takes part. Lengths are loaded kPrefixBatch tiles at a time so that their latencies overlap.
+// wsum: 64 ints of smem.
 constexpr int kPrefixBatch = 8;
 
-__device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref, int32_t* ipref, int32_t* wsum) {
+__device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref, int32_t* ipref, int32_t* cfirst,
+                                             int32_t* wsum) {
   const int32_t n = a.n_seqs;
   const int32_t PC = a.part_chunks > 0 ? a.part_chunks : 1;
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
@@ -155,7 +159,8 @@ __device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref,
         record_error(ERRBIT_BOUNDS);
         len = len < 0 ? 0 : cap;
       }
-      const int32_t c = (len + kChunk - 1) / kChunk;
+      const int32_t c0 = (a.window > 0 && len > a.window) ? (len - a.window) / kChunk : 0;
+      const int32_t c = (len + kChunk - 1) / kChunk - c0;
       const int32_t ci = (c + PC - 1) / PC;
       int32_t ic = c, ii = ci;  // inclusive warp scan
 #pragma unroll
@@ -186,6 +191,7 @@ __device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref,
       if (b < n) {
         pref[b] = carry_c + pc + ic - c;
         ipref[b] = carry_i + pi + ii - ci;
+        cfirst[b] = c0;
       }
       carry_c += tc;
       carry_i += ti;
@@ -258,7 +264,8 @@ struct SimtMath {
     }
   }
 
-  __device__ static void chunk(Regs& r, const unsigned char* kb, int nvalid, float, int lane) {
+  // Tokens vlo <= tok < vhi of the chunk are inside the attention range; the rest are masked.
+  __device__ static void chunk(Regs& r, const unsigned char* kb, int vlo, int vhi, float, int lane) {
     const unsigned char* vb = kb + CB;
     const int tg = lane / LPT;
     const int cl = lane % LPT;
@@ -277,7 +284,7 @@ struct SimtMath {
         for (int e = 0; e < EPL; ++e) s = fmaf(r.q[j][e], kf[e], s);
 #pragma unroll
         for (int off = LPT / 2; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        sc[p][j] = tok < nvalid ? s : -INFINITY;
+        sc[p][j] = (tok >= vlo && tok < vhi) ? s : -INFINITY;
       }
     }
 #pragma unroll
@@ -304,7 +311,7 @@ struct SimtMath {
 #pragma unroll
     for (int p = 0; p < PASSES; ++p) {
       const int tok = p * TPP + tg;
-      if (tok < nvalid) {   // values past the context may be garbage (even NaN): never touch them
+      if (tok >= vlo && tok < vhi) {   // values outside the range may be garbage (even NaN)
         float vf[EPL];
 #pragma unroll
         for (int pc = 0; pc < PIECES; ++pc)
@@ -417,7 +424,8 @@ struct MmaMath {
     return static_cast<uint32_t>(row * 128 + ((cb ^ (row & 7)) << 4));
   }
 
-  __device__ static void chunk(Regs& r, const unsigned char* kbase, int nvalid, float scale_log2, int lane) {
+  // Tokens vlo <= tok < vhi of the chunk are inside the attention range; the rest are masked.
+  __device__ static void chunk(Regs& r, const unsigned char* kbase, int vlo, int vhi, float scale_log2, int lane) {
     const uint32_t kb = smem_addr(kbase);
     const uint32_t vb = kb + CB;
     const int t = lane & 3;
@@ -439,10 +447,12 @@ struct MmaMath {
     }
     // ---- online softmax for head g over tokens {2t, 2t+1, 8+2t, 9+2t}
     float x[4];
-    x[0] = (2 * t < nvalid) ? s[0][0] * scale_log2 : -INFINITY;
-    x[1] = (2 * t + 1 < nvalid) ? s[0][1] * scale_log2 : -INFINITY;
-    x[2] = (8 + 2 * t < nvalid) ? s[1][0] * scale_log2 : -INFINITY;
-    x[3] = (9 + 2 * t < nvalid) ? s[1][1] * scale_log2 : -INFINITY;
+    const bool ok0 = 2 * t >= vlo && 2 * t < vhi, ok1 = 2 * t + 1 >= vlo && 2 * t + 1 < vhi;
+    const bool ok2 = 8 + 2 * t >= vlo && 8 + 2 * t < vhi, ok3 = 9 + 2 * t >= vlo && 9 + 2 * t < vhi;
+    x[0] = ok0 ? s[0][0] * scale_log2 : -INFINITY;
+    x[1] = ok1 ? s[0][1] * scale_log2 : -INFINITY;
+    x[2] = ok2 ? s[1][0] * scale_log2 : -INFINITY;
+    x[3] = ok3 ? s[1][1] * scale_log2 : -INFINITY;
     float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -470,9 +480,9 @@ struct MmaMath {
     const uint32_t lo1 = pack_bf16x2(pr[2] - bf16_lo(hi1), pr[3] - bf16_hi(hi1));
     // ---- O += P V (rows 0..7: hi, rows 8..15: lo)
     uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
-    if (nvalid < kChunk) {  // zero V entries of tokens past the context (they may hold NaN)
-      mask01 = ((2 * t < nvalid) ? 0x0000ffffu : 0u) | ((2 * t + 1 < nvalid) ? 0xffff0000u : 0u);
-      mask23 = ((8 + 2 * t < nvalid) ? 0x0000ffffu : 0u) | ((9 + 2 * t < nvalid) ? 0xffff0000u : 0u);
+    if (vlo > 0 || vhi < kChunk) {  // zero V entries of tokens outside the range (they may hold NaN)
+      mask01 = (ok0 ? 0x0000ffffu : 0u) | (ok1 ? 0xffff0000u : 0u);
+      mask23 = (ok2 ? 0x0000ffffu : 0u) | (ok3 ? 0xffff0000u : 0u);
     }
     const int vtok = mr + 8 * (mi & 1);
 #pragma unroll
@@ -525,9 +535,10 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
   int32_t* wsum = reinterpret_cast<int32_t*>(smem + decode_ring_bytes(NW, S, SB) + static_cast<size_t>(NW) * S * 8);
   int32_t* pref = wsum + 64;
   int32_t* ipref = pref + (n + 1);
+  int32_t* cfirst = ipref + (n + 1);
 
   pdl_wait();
-  build_prefix(a, pref, ipref, wsum);
+  build_prefix(a, pref, ipref, cfirst, wsum);
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
     fence_mbar_init();
@@ -570,7 +581,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
   int64_t issued = 0;
 
   auto issue = [&](int stage) {
-    const int32_t tok0 = pf.c * kChunk;
+    const int32_t tok0 = (cfirst[pf.b] + pf.c) * kChunk;
     const int32_t pg = tok0 / a.B;
     if (pf.b != win_b || pg < win_base || pg >= win_base + 32) {
       win_b = pf.b;
@@ -629,8 +640,10 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
       aborted = true;
       break;
     }
-    const int32_t nvalid = min(kChunk, len_b - cc.c * kChunk);
-    Math::chunk(r, ring + static_cast<size_t>(stage) * SB, nvalid, a.scale_log2, lane);
+    const int32_t tok_abs = (cfirst[cc.b] + cc.c) * kChunk;
+    const int32_t vhi = min(kChunk, len_b - tok_abs);
+    const int32_t vlo = a.window > 0 ? max(0, len_b - a.window - tok_abs) : 0;
+    Math::chunk(r, ring + static_cast<size_t>(stage) * SB, vlo, vhi, a.scale_log2, lane);
     __syncwarp();
     if (issued < n_chunks) issue(stage);
 
@@ -702,7 +715,9 @@ __global__ void __launch_bounds__(32 * kReduceWarps) decode_reduce_kernel(const 
     }
     n_parts = w_last - first_slot + 1;
   } else {
-    const int32_t nch = (clamped_len(a, b) + kChunk - 1) / kChunk;
+    const int32_t len = clamped_len(a, b);
+    const int32_t c0 = (a.window > 0 && len > a.window) ? (len - a.window) / kChunk : 0;
+    const int32_t nch = (len + kChunk - 1) / kChunk - c0;
     n_parts = (nch + a.part_chunks - 1) / a.part_chunks;
     if (n_parts <= 1) return;
     if (n_parts > a.max_parts) {

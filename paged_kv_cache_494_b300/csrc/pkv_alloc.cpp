@@ -162,7 +162,7 @@ pkv_status pkv_alloc(pkv_pool* p, int32_t seq, int32_t n_tokens, int32_t* seq_ou
   } else {
     if (seq < 0 || seq >= p->desc.max_seqs || !p->live[seq]) return PKV_ERR_NO_SEQ;
     len = p->lens[seq];
-    if (!p->tables[seq].empty()) rc_last = p->refcount[p->tables[seq].back()];
+    if (!p->tables[seq].empty() && p->tables[seq].back() >= 0) rc_last = p->refcount[p->tables[seq].back()];
   }
   const int64_t new_len = static_cast<int64_t>(len) + n_tokens;
   if (ceil_div(new_len, B) > p->desc.max_blocks_per_seq) return PKV_ERR_CAPACITY;
@@ -207,7 +207,7 @@ pkv_status pkv_append(pkv_pool* p, const int32_t* seqs, int32_t n, int64_t* slot
     const int32_t s = seqs[i];
     const int32_t len = p->lens[s];
     int32_t rc_last = 0, last = -1;
-    if (!p->tables[s].empty()) {
+    if (!p->tables[s].empty() && p->tables[s].back() >= 0) {   // a released last block is a hole (-1)
       last = p->tables[s].back();
       rc_last = p->refcount[last] + rc_delta[last];
     }
@@ -232,7 +232,8 @@ pkv_status pkv_fork(pkv_pool* p, int32_t parent, int32_t* child_out) {
   p->live[c] = 1;
   p->tables[c] = p->tables[parent];
   p->lens[c] = p->lens[parent];
-  for (int32_t b : p->tables[c]) add_ref(p, b);
+  for (int32_t b : p->tables[c])
+    if (b >= 0) add_ref(p, b);   // released (sliding-window) entries stay holes
   p->n_tokens += p->lens[c];
   *child_out = c;
   return PKV_OK;
@@ -242,12 +243,29 @@ pkv_status pkv_free(pkv_pool* p, int32_t seq) {
   if (!p) return PKV_ERR_INVALID;
   if (seq < 0 || seq >= p->desc.max_seqs || !p->live[seq]) return PKV_ERR_NO_SEQ;
   for (int32_t b : p->tables[seq])
-    if (drop_ref(p, b)) p->free_stack.push_back(b);
+    if (b >= 0 && drop_ref(p, b)) p->free_stack.push_back(b);
   p->n_tokens -= p->lens[seq];
   p->tables[seq].clear();
   p->lens[seq] = 0;
   p->live[seq] = 0;
   p->free_ids.insert(seq);
+  return PKV_OK;
+}
+
+pkv_status pkv_release_before(pkv_pool* p, int32_t seq, int32_t position, int32_t* n_released_out) {
+  if (!p) return PKV_ERR_INVALID;
+  if (seq < 0 || seq >= p->desc.max_seqs || !p->live[seq]) return PKV_ERR_NO_SEQ;
+  if (position < 0 || position > p->lens[seq]) return PKV_ERR_INVALID;
+  const int32_t B = p->desc.block_size;
+  std::vector<int32_t>& t = p->tables[seq];
+  int32_t released = 0;
+  for (int32_t i = 0; i < static_cast<int32_t>(t.size()) && static_cast<int64_t>(i + 1) * B <= position; ++i) {
+    if (t[i] < 0) continue;
+    if (drop_ref(p, t[i])) p->free_stack.push_back(t[i]);
+    t[i] = -1;
+    ++released;
+  }
+  if (n_released_out) *n_released_out = released;
   return PKV_OK;
 }
 

@@ -297,7 +297,15 @@ pkv_status pkv_paged_decode(const pkv_pool* p, float* out, const void* q, const 
                             const int32_t* block_tables, const int32_t* context_lens, int32_t n_seqs,
                             int32_t num_q_heads, float scale, int32_t partition_tokens, void* workspace,
                             size_t workspace_bytes, void* stream) {
-  if (!p) return PKV_ERR_INVALID;
+  return pkv_paged_decode_window(p, out, q, k_cache, v_cache, block_tables, context_lens, n_seqs, num_q_heads, scale,
+                                 0, partition_tokens, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_decode_window(const pkv_pool* p, float* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                                   int32_t n_seqs, int32_t num_q_heads, float scale, int32_t window,
+                                   int32_t partition_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p || window < 0) return PKV_ERR_INVALID;
   if (n_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
@@ -331,6 +339,7 @@ pkv_status pkv_paged_decode(const pkv_pool* p, float* out, const void* q, const 
   a.max_parts = pl.max_parts;
   a.stages = pl.stages;
   a.total_warps = pl.warps;
+  a.window = window;
   a.scale_log2 = scale * 1.4426950408889634f;
   pkv_dev::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);

@@ -171,9 +171,19 @@ class Case:
         self.oracle_lens = np.asarray(mlens, dtype=np.int32)
 
     # -- running -----------------------------------------------------------------------------
+    def refresh_tables(self):
+        """Re-export both sides' block tables (after releases); they must agree bit-exactly."""
+        tables, lens = self.pool.block_table(self.seqs)
+        mtab, mlens = self.model.block_table(self.seqs)
+        assert tables.tolist() == mtab and lens.tolist() == mlens
+        self.tables = torch.from_numpy(tables).cuda()
+        self.lens = torch.from_numpy(lens).cuda()
+        self.oracle_tables = np.asarray(mtab, dtype=np.int32)
+        self.oracle_lens = np.asarray(mlens, dtype=np.int32)
+
     def gpu_decode(self, partition_tokens: int = 0, q: Optional[torch.Tensor] = None,
                    tables: Optional[torch.Tensor] = None, lens: Optional[torch.Tensor] = None,
-                   k_cache=None, v_cache=None) -> torch.Tensor:
+                   k_cache=None, v_cache=None, window: int = 0) -> torch.Tensor:
         q = self.q if q is None else q
         out = torch.full((self.n, self.Hq, self.D), float("nan"), dtype=torch.float32, device="cuda")
         nbytes = self.pool.decode_workspace_bytes(self.n, self.Hq, partition_tokens)
@@ -181,14 +191,14 @@ class Case:
         self.pool.paged_decode(out, q, self.k_cache if k_cache is None else k_cache,
                                self.v_cache if v_cache is None else v_cache,
                                self.tables if tables is None else tables, self.lens if lens is None else lens,
-                               self.scale, partition_tokens=partition_tokens, workspace=ws)
+                               self.scale, partition_tokens=partition_tokens, workspace=ws, window=window)
         torch.cuda.synchronize()
         return out
 
-    def oracle_decode(self, rows: Optional[List[int]] = None) -> np.ndarray:
+    def oracle_decode(self, rows: Optional[List[int]] = None, window: int = 0) -> np.ndarray:
         assert self.host_cache
         return native.decode(self.q_stored, self.hk, self.hv, self.oracle_tables, self.oracle_lens, self.scale,
-                             rows=rows)
+                             rows=rows, window=window)
 
 
 def case_from_workload(name: str, seed: Optional[int] = None, host_cache: bool = True,

@@ -52,9 +52,13 @@ def drive(seed, NB, B, max_seqs, MB, n_ops, fail_after=-1, max_append=40):
             a = lib.append_raw(seqs)
             b = m.append(seqs)
             assert a[0] == b[0] and a[1].tolist() == b[1] and [tuple(p) for p in a[2].tolist()] == b[2]
-        elif r < 0.8:
+        elif r < 0.75:
             s = int(rng.choice(live))
             assert lib.fork_raw(s) == m.fork(s)
+        elif r < 0.8:
+            s = int(rng.choice(live))
+            pos = int(rng.integers(0, m.lens[s] + 2))
+            assert lib.release_before_raw(s, pos) == m.release_before(s, pos)
         else:
             s = int(rng.choice(live)) if rng.random() < 0.97 else int(rng.integers(0, max_seqs + 2))
             assert lib.free_raw(s) == m.free_seq(s)

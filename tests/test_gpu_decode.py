@@ -149,3 +149,38 @@ def test_host_argument_checks():
         c.pool.paged_decode(out, c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, partition_tokens=24)
     odd = pkv.Pool(1, 2, 128, 8, 16, 2, 8, pkv.BF16)     # block size 8 is not supported by the kernels
     assert odd.decode_workspace_bytes(1, 8) == 0
+
+
+@pytest.mark.parametrize("window", [1, 16, 37, 100, 5000])
+@pytest.mark.parametrize("partition_tokens", [0, 64])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_sliding_window_parity(window, partition_tokens, dtype, path):
+    if dtype == "f32" and path == "simt":
+        pytest.skip("fp32 always runs on the CUDA-core path")
+    c = Case(lengths=[0, 1, 15, 16, 17, 100, 257, 700, 1500], Hq=32, Hkv=8, D=128, B=16, dtype=dtype, seed=71)
+    out = c.gpu_decode(partition_tokens, window=window)
+    check(c, out, c.oracle_decode(window=window))
+    assert pkv.last_error() == pkv.OK
+
+
+def test_window_with_released_blocks(path):
+    """Blocks wholly before the window are released (holes in the tables) and never read."""
+    W = 128
+    c = Case(lengths=[300, 1000, 40, 129, 16 * 9], Hq=32, Hkv=8, D=128, B=16, dtype="bf16", seed=73)
+    before = c.pool.stats()["num_free"]
+    released = 0
+    for sid, L in zip(c.seqs, c.oracle_lens.tolist()):
+        released += c.pool.release_before(sid, max(0, L - W))
+        st, n = c.model.release_before(sid, max(0, L - W))
+        assert st == 0
+    c.refresh_tables()
+    assert released > 0 and c.pool.stats()["num_free"] == before + released
+    assert (c.oracle_tables == -1).any()
+    for pt in (0, 32):
+        check(c, c.gpu_decode(pt, window=W), c.oracle_decode(window=W))
+    assert pkv.last_error() == pkv.OK
+    # appends keep working after a release, and the window keeps sliding
+    for _ in range(20):
+        c.decode_step_append()
+    check(c, c.gpu_decode(0, window=W), c.oracle_decode(window=W))
+    assert pkv.last_error() == pkv.OK

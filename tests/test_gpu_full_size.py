@@ -28,6 +28,14 @@ def test_serve256_one_layer_full():
     assert pkv.last_error() == pkv.OK
 
 
+def test_serve256_one_layer_sliding_window():
+    c = case_from_workload("serve256_bf16")
+    out = c.gpu_decode(0, window=256)
+    err = float(np.max(np.abs(out.double().cpu().numpy() - c.oracle_decode(window=256))))
+    assert err <= TOL["bf16"]
+    assert pkv.last_error() == pkv.OK
+
+
 def test_long_split_full():
     c = case_from_workload("long_split_bf16", compact_host=True)
     assert c.NB > 600_000

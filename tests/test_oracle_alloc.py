@@ -16,7 +16,8 @@ def check_invariants(p: am.PoolModel):
     counts = [0] * p.NB
     for t in p.tables.values():
         for b in t:
-            counts[b] += 1
+            if b >= 0:
+                counts[b] += 1
     assert counts == p.refcount
     assert len(set(p.free)) == len(p.free)
     assert all(p.refcount[b] == 0 for b in p.free)
@@ -45,7 +46,7 @@ class Memory:
 
     def read(self, seq):
         t, L, B = self.p.tables[seq], self.p.lens[seq], self.p.B
-        return [self.slot.get(t[i // B] * B + i % B) for i in range(L)]
+        return [self.slot.get(t[i // B] * B + i % B) if t[i // B] >= 0 else "released" for i in range(L)]
 
 
 def random_ops(seed, p: am.PoolModel, n_ops, max_append=40):
@@ -61,9 +62,13 @@ def random_ops(seed, p: am.PoolModel, n_ops, max_append=40):
             s = int(rng.choice(live))
             n = int(rng.integers(0, max_append))
             yield ("alloc", s, n), p.alloc(s, n)
-        elif r < 0.8:
+        elif r < 0.75:
             s = int(rng.choice(live))
             yield ("fork", s), p.fork(s)
+        elif r < 0.8:
+            s = int(rng.choice(live))
+            pos = int(rng.integers(0, p.lens[s] + 1))
+            yield ("release", s, pos), p.release_before(s, pos)
         else:
             s = int(rng.choice(live))
             yield ("free", s), p.free_seq(s)
@@ -96,6 +101,11 @@ def test_isolation_and_order(seed, B):
             st, child = res
             if st == am.OK:
                 history[child] = list(history[op[1]])
+        elif op[0] == "release":
+            assert res[0] == am.OK
+            B_ = p.B
+            history[op[1]] = ["released" if (i // B_ + 1) * B_ <= op[2] or h == "released" else h
+                              for i, h in enumerate(history[op[1]])]
         else:
             assert res == am.OK
             history.pop(op[1])
@@ -238,3 +248,20 @@ def test_handout_order_and_lifo_reuse():
     p.free_seq(a)
     _, c, _, _ = p.alloc(-1, 1)
     assert p.tables[c] == [7]               # the last block freed is handed out first
+
+
+def test_release_before_frees_only_unshared_blocks():
+    p = am.PoolModel(64, 16, 8, 16)
+    _, a, _, _ = p.alloc(-1, 100)              # 7 blocks
+    _, c = p.fork(a)
+    st, n = p.release_before(a, 50)             # blocks 0..2 lie entirely before position 50
+    assert st == am.OK and n == 3 and p.tables[a][:3] == [-1, -1, -1]
+    assert all(p.refcount[b] == 1 for b in p.tables[c][:3])   # still held by the fork
+    assert p.stats()["num_free"] == 64 - 7
+    p.free_seq(c)
+    assert p.stats()["num_free"] == 64 - 4     # the released blocks are free once nobody holds them
+    assert p.release_before(a, 101) == (am.ERR_INVALID, 0)
+    check_invariants(p)
+    # appends continue at the same slots after a release
+    st, _, slots, _ = p.alloc(a, 1)
+    assert st == am.OK and slots == [p.tables[a][6] * 16 + 100 % 16]

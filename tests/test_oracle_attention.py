@@ -21,8 +21,8 @@ from oracle import attention as att
 from oracle import native
 
 IMPLS = {
-    "numpy": lambda *a: att.paged_decode(*a),
-    "c": lambda *a: native.decode(*a),
+    "numpy": lambda *a, **k: att.paged_decode(*a, **k),
+    "c": lambda *a, **k: native.decode(*a, **k),
 }
 
 
@@ -243,3 +243,33 @@ def test_c_oracle_sampled_rows_and_threads():
     part = native.decode(P["q"], P["kc"], P["vc"], P["tables"], P["lens"], P["scale"], rows=rows)
     for r, flat in enumerate(rows):
         assert np.array_equal(part[r], full[flat // 8, flat % 8])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_sliding_window(impl):
+    """Window W: the last W positions only. W >= len is full attention; W = 1 returns the last V
+    row; otherwise it equals SDPA on the sliced logical K/V."""
+    P = make_problem(81, [300, 40, 1, 17], 8, 2, 64, 16, "bf16")
+    full = run(impl, P)
+    run_w = lambda W: IMPLS[impl](P["q"], P["kc"], P["vc"], P["tables"], P["lens"], P["scale"], window=W)
+    assert np.array_equal(run_w(300), full) and np.array_equal(run_w(10_000), full)
+    one = run_w(1)
+    for b, L in enumerate(P["lens"]):
+        for j in range(8):
+            assert np.array_equal(one[b, j], att.to_f64(P["logical"][b][1][L - 1, j // 4]))
+    for W in (16, 33, 100):
+        sl = dict(P)
+        sl["logical"] = [(k[-W:], v[-W:]) for k, v in P["logical"]]
+        np.testing.assert_allclose(run_w(W), sdpa(sl), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_window_ignores_released_blocks(impl):
+    """Blocks entirely before the window may be released (table entry -1): never read."""
+    P = make_problem(83, [300, 100], 8, 2, 64, 16, "f32")
+    ref = IMPLS[impl](P["q"], P["kc"], P["vc"], P["tables"], P["lens"], P["scale"], window=64)
+    holes = P["tables"].copy()
+    holes[0, :(300 - 64) // 16] = -1
+    holes[1, :(100 - 64) // 16] = -1
+    out = IMPLS[impl](P["q"], P["kc"], P["vc"], holes, P["lens"], P["scale"], window=64)
+    assert np.array_equal(out, ref)

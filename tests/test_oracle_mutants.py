@@ -29,6 +29,14 @@ def pin_checks(fn):
         if not all(np.array_equal(o1[b, j], att.to_f64(P1["logical"][b][1][0, j // 4]))
                    for b in range(2) for j in range(8)):
             failed.append("single_token")
+        if getattr(fn, "supports_window", False):
+            Pw = make_problem(17, [300, 40], 8, 2, 64, 16, "bf16")
+            ow = fn(Pw["q"], Pw["kc"], Pw["vc"], Pw["tables"], Pw["lens"], Pw["scale"], window=50)
+            sl = dict(Pw)
+            sl["logical"] = [(k[-50:], v[-50:]) for k, v in Pw["logical"]]
+            sl["lens"] = np.minimum(Pw["lens"], 50)
+            if not np.allclose(ow, sdpa(sl), rtol=0, atol=1e-12):
+                failed.append("window")
         Px = make_problem(13, [300, 7], 8, 2, 64, 16, "f32")
         Px["q"] = (Px["q"] * 100.0).astype(np.float32)
         ox = fn(Px["q"], Px["kc"], Px["vc"], Px["tables"], Px["lens"], Px["scale"])
@@ -79,9 +87,14 @@ def _mutant(kind):
     return decode
 
 
+def _windowed(fn):
+    fn.supports_window = True
+    return fn
+
+
 def test_unmodified_oracles_pass_every_pin():
-    assert pin_checks(att.paged_decode) == []
-    assert pin_checks(native.decode) == []
+    assert pin_checks(_windowed(lambda *a, **k: att.paged_decode(*a, **k))) == []
+    assert pin_checks(_windowed(lambda *a, **k: native.decode(*a, **k))) == []
 
 
 @pytest.mark.parametrize("kind", ["block_index", "offset", "drop_last", "no_scale", "no_max", "no_norm",
@@ -93,7 +106,8 @@ def test_numpy_mutant_is_caught(kind):
 # ---- C mutants: one textual edit of decode_ref.c, built into a temporary directory ------------------
 
 C_MUTANTS = {
-    "offset": ("(t % block_size)) * D;", "(block_size - 1 - t % block_size)) * D;"),
+    "offset": ("(pos % block_size)) * D;", "(block_size - 1 - pos % block_size)) * D;"),
+    "window_off_by_one": ("? len - window : 0;", "? len - window + 1 : 0;"),
     "gqa_mod": ("const int h = j / g;", "const int h = j % num_kv_heads;"),
     "no_scale": ("s[t] = scale * acc;", "s[t] = acc;"),
     "no_max": ("s[t] = exp(s[t] - m);", "s[t] = exp(s[t]);"),
@@ -113,4 +127,4 @@ def test_c_mutant_is_caught(kind, tmp_path):
     mpath.write_text(src.replace(old, new))
     so = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-o", str(so), str(mpath), "-lm"], check=True)
-    assert pin_checks(native.decode_fn_from(str(so))) != []
+    assert pin_checks(_windowed(native.decode_fn_from(str(so)))) != []
