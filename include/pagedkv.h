@@ -151,6 +151,35 @@ PKV_API pkv_status pkv_free(pkv_pool* pool, int32_t seq);
  * Errors: NO_SEQ, INVALID (position out of range). */
 PKV_API pkv_status pkv_release_before(pkv_pool* pool, int32_t seq, int32_t position, int32_t* n_released_out);
 
+/* ---- prefix cache (host only) ------------------------------------------------------------- */
+/* Prompt blocks are shared by content ("Servicio de modelos de lenguaje con un presupuesto de
+ * memoria" §8: the key must cover every input that affects the state, reused pages must never
+ * expose another request's continuation, eviction must not free pages in use; "PagedAttention e
+ * vLLM", "Implementazione nel mondo reale": a shared system prompt is processed once).
+ * The key of prompt block i is (cache_namespace, the cache entry of block i-1, the B token ids of
+ * block i); the caller folds the model version and every configuration value that changes K/V into
+ * cache_namespace. Only full blocks are cached; a lookup stops at the first miss. Entry ids are never
+ * reused, so entries whose parent was evicted can no longer be reached. The cache holds one reference
+ * on each cached block; a cached block held by nothing else is evictable. */
+
+/* New sequence for the prompt tokens[0..n_tokens): the leading full blocks found in the cache are
+ * shared (refcount + 1); the rest are taken from the free list and the full ones are registered.
+ * Outputs: *seq_out; slots_out[n_tokens]; *n_cached_out = number of leading positions whose K/V is
+ * already in the cache (a multiple of B) — the caller writes K/V only for positions >= that (and must
+ * order those writes before any read of the newly registered blocks, e.g. on one stream).
+ * Check order: CAPACITY (no id, or too many blocks), injected failure, NO_BLOCKS (free list too short;
+ * the cache is not evicted implicitly). All-or-nothing. */
+PKV_API pkv_status pkv_alloc_prefix(pkv_pool* pool, uint64_t cache_namespace, const int32_t* tokens,
+                                    int32_t n_tokens, int32_t* seq_out, int64_t* slots_out, int32_t* n_cached_out);
+
+/* Evict up to max_blocks evictable cached blocks, in the order they became evictable (oldest first):
+ * each leaves the cache and goes on top of the free list. Blocks any sequence still holds are never
+ * evicted. *n_evicted_out (may be NULL) = blocks evicted. */
+PKV_API pkv_status pkv_prefix_evict(pkv_pool* pool, int32_t max_blocks, int32_t* n_evicted_out);
+
+/* Number of cached blocks and of evictable ones (either output may be NULL). */
+PKV_API pkv_status pkv_prefix_stats(const pkv_pool* pool, int32_t* n_cached_blocks, int32_t* n_evictable);
+
 /* Host copies of the block tables of n live sequences: table_out[n][max_blocks_per_seq]
  * (int32, unused entries -1) and lens_out[n]. Either output may be NULL. */
 PKV_API pkv_status pkv_block_table(const pkv_pool* pool, const int32_t* seqs, int32_t n, int32_t* table_out,

@@ -229,3 +229,128 @@ class PoolModel:
             "num_seqs": len(self.tables),
             "num_tokens": sum(self.lens.values()),
         }
+
+
+class PrefixCacheModel(PoolModel):
+    """The pool plus a cache of full prompt blocks keyed by their content (integers, dictionaries).
+
+    What the pages fix: "Servicio de modelos de lenguaje con un presupuesto de memoria" §8 — a cache
+    key must identify every input that affects the state (model version, relevant configuration);
+    reused pages must not expose another request's private continuation nor let it modify shared
+    state; cancellation and eviction release references without freeing pages in use. "PagedAttention
+    e vLLM", "Implementazione nel mondo reale" — a long system prompt shared by many requests is
+    processed once. "Paged Attention optimiza el uso de memoria en LLMs" — requests that start from
+    the same point use the same physical pages until they diverge.
+
+    Readings (the library's ABI follows them):
+    * key of prompt block i = (namespace, key entry of block i-1 (None for i = 0), the B token ids);
+      only full blocks are cached; a lookup stops at the first miss;
+    * each cache entry gets an id that is never reused; children refer to their parent by that id, so
+      an entry whose parent was evicted can never be hit again;
+    * the cache holds one reference on each cached block; when that is the last reference the block
+      becomes evictable (queue order = the order in which blocks became evictable; a hit removes it);
+    * evict(n) removes up to n evictable blocks, oldest first, and frees them.
+    """
+
+    def __init__(self, *args, **kwargs):
+        super().__init__(*args, **kwargs)
+        self.entries = {}          # (ns, parent_entry_id, tokens) -> (entry_id, block)
+        self.entry_of_block = {}   # block -> key
+        self.next_entry = 0
+        self.evictable = []        # blocks whose only reference is the cache, oldest first
+
+    def _drop(self, b: int):
+        """One reference fewer on block b (shared by free_seq / release_before when caching)."""
+        self.refcount[b] -= 1
+        if self.refcount[b] == 0:
+            self.free.append(b)
+        elif self.refcount[b] == 1 and b in self.entry_of_block:
+            self.evictable.append(b)
+
+    def free_seq(self, seq: int) -> int:
+        if seq not in self.tables:
+            return ERR_NO_SEQ
+        for b in self.tables.pop(seq):
+            if b >= 0:
+                self._drop(b)
+        del self.lens[seq]
+        return OK
+
+    def release_before(self, seq: int, position: int):
+        if seq not in self.tables:
+            return ERR_NO_SEQ, 0
+        if position < 0 or position > self.lens[seq]:
+            return ERR_INVALID, 0
+        t = self.tables[seq]
+        released = 0
+        for i in range(len(t)):
+            if (i + 1) * self.B > position:
+                break
+            if t[i] < 0:
+                continue
+            self._drop(t[i])
+            t[i] = -1
+            released += 1
+        return OK, released
+
+    def alloc_prefix(self, ns: int, tokens):
+        """New sequence holding the prompt ``tokens``. Returns (status, seq, slots, n_cached_tokens):
+        the K/V of positions < n_cached_tokens are already in cached blocks; the caller writes the rest."""
+        tokens = [int(x) for x in tokens]
+        n, B = len(tokens), self.B
+        sid = self._new_id()
+        if sid < 0:
+            return ERR_CAPACITY, -1, [], 0
+        if -(-n // B) > self.MB:
+            return ERR_CAPACITY, -1, [], 0
+        if self.fail_after >= 0 and self.n_allocs >= self.fail_after:
+            return ERR_NO_BLOCKS, -1, [], 0
+        # walk the cache: the leading full blocks that hit
+        hits, parent = [], None
+        for i in range(n // B):
+            key = (ns, parent, tuple(tokens[i * B:(i + 1) * B]))
+            if key not in self.entries:
+                break
+            eid, blk = self.entries[key]
+            hits.append(blk)
+            parent = eid
+        need = -(-n // B) - len(hits)
+        if need > len(self.free):
+            return ERR_NO_BLOCKS, -1, [], 0
+        # commit: shared blocks first, then fresh blocks (full ones are registered)
+        table = []
+        for blk in hits:
+            if self.refcount[blk] == 1:
+                self.evictable.remove(blk)
+            self.refcount[blk] += 1
+            table.append(blk)
+        for i in range(len(hits), -(-n // B)):
+            blk = self._pop()
+            table.append(blk)
+            if (i + 1) * B <= n:
+                key = (ns, parent, tuple(tokens[i * B:(i + 1) * B]))
+                self.entries[key] = (self.next_entry, blk)
+                self.entry_of_block[blk] = key
+                parent = self.next_entry
+                self.next_entry += 1
+                self.refcount[blk] += 1          # the cache's own reference
+        self.tables[sid] = table
+        self.lens[sid] = n
+        self.n_allocs += 1
+        slots = [table[t // B] * B + t % B for t in range(n)]
+        return OK, sid, slots, len(hits) * B
+
+    def evict(self, max_blocks: int) -> int:
+        """Remove up to max_blocks evictable blocks from the cache (oldest first) and free them."""
+        n = 0
+        while n < max_blocks and self.evictable:
+            blk = self.evictable.pop(0)
+            key = self.entry_of_block.pop(blk)
+            del self.entries[key]
+            self.refcount[blk] -= 1
+            self.free.append(blk)
+            n += 1
+        return n
+
+    def prefix_stats(self):
+        return len(self.entries), len(self.evictable)

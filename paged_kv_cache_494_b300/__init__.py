@@ -63,6 +63,9 @@ _SIGS = {
     "pkv_free": (ctypes.c_int, [_vp, _i32]),
     "pkv_block_table": (ctypes.c_int, [_vp, _pi32, _i32, _pi32, _pi32]),
     "pkv_release_before": (ctypes.c_int, [_vp, _i32, _i32, _pi32]),
+    "pkv_alloc_prefix": (ctypes.c_int, [_vp, ctypes.c_uint64, _pi32, _i32, _pi32, _pi64, _pi32]),
+    "pkv_prefix_evict": (ctypes.c_int, [_vp, _i32, _pi32]),
+    "pkv_prefix_stats": (ctypes.c_int, [_vp, _pi32, _pi32]),
     "pkv_pool_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
     "pkv_export_state": (ctypes.c_int, [_vp, _pi32, _pi32, _pi32]),
     "pkv_reshape_and_cache": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp]),
@@ -236,6 +239,33 @@ class Pool:
         st, n = self.release_before_raw(seq, position)
         _check(st, "pkv_release_before")
         return n
+
+    def alloc_prefix_raw(self, namespace: int, tokens: Sequence[int]) -> Tuple[int, int, np.ndarray, int]:
+        """pkv_alloc_prefix without raising: (status, seq, slots, n_cached_tokens)."""
+        tok = np.ascontiguousarray(list(tokens), dtype=np.int32)
+        slots = np.zeros(max(tok.size, 1), dtype=np.int64)
+        sid, ncached = _i32(-1), _i32(0)
+        st = lib.pkv_alloc_prefix(self._h, ctypes.c_uint64(int(namespace) & 0xFFFFFFFFFFFFFFFF),
+                                  _i32p(tok) if tok.size else None, tok.size, ctypes.byref(sid), _i64p(slots),
+                                  ctypes.byref(ncached))
+        if st != OK:
+            return st, -1, np.zeros(0, dtype=np.int64), 0
+        return st, sid.value, slots[:tok.size], ncached.value
+
+    def alloc_prefix(self, namespace: int, tokens: Sequence[int]) -> Tuple[int, np.ndarray, int]:
+        st, sid, slots, ncached = self.alloc_prefix_raw(namespace, tokens)
+        _check(st, "pkv_alloc_prefix")
+        return sid, slots, ncached
+
+    def prefix_evict(self, max_blocks: int) -> int:
+        n = _i32(0)
+        _check(lib.pkv_prefix_evict(self._h, int(max_blocks), ctypes.byref(n)), "pkv_prefix_evict")
+        return n.value
+
+    def prefix_stats(self) -> Tuple[int, int]:
+        a, b = _i32(0), _i32(0)
+        _check(lib.pkv_prefix_stats(self._h, ctypes.byref(a), ctypes.byref(b)), "pkv_prefix_stats")
+        return a.value, b.value
 
     def block_table(self, seqs: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
         s = np.ascontiguousarray(list(seqs), dtype=np.int32)

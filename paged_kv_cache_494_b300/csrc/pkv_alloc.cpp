@@ -29,11 +29,18 @@ void add_ref(pkv_pool* p, int32_t b) {
   r++;
 }
 
-// Returns true when the block became free.
+// Returns true when the block became free. A cached block left with only the cache's reference
+// becomes evictable.
 bool drop_ref(pkv_pool* p, int32_t b) {
   int32_t& r = p->refcount[b];
   r--;
-  if (r == 1) p->n_shared--;
+  if (r == 1) {
+    p->n_shared--;
+    if (!p->prefix_key_of_block.empty() && p->prefix_key_of_block.count(b)) {
+      p->evictable.push_back(b);
+      p->evictable_pos[b] = std::prev(p->evictable.end());
+    }
+  }
   if (r == 0) {
     p->n_used--;
     return true;
@@ -266,6 +273,90 @@ pkv_status pkv_release_before(pkv_pool* p, int32_t seq, int32_t position, int32_
     ++released;
   }
   if (n_released_out) *n_released_out = released;
+  return PKV_OK;
+}
+
+pkv_status pkv_alloc_prefix(pkv_pool* p, uint64_t ns, const int32_t* tokens, int32_t n_tokens, int32_t* seq_out,
+                            int64_t* slots_out, int32_t* n_cached_out) {
+  if (!p || !seq_out || !n_cached_out || n_tokens < 0 || (n_tokens > 0 && (!tokens || !slots_out)))
+    return PKV_ERR_INVALID;
+  const int32_t B = p->desc.block_size;
+  if (p->free_ids.empty()) return PKV_ERR_CAPACITY;
+  const int32_t nblk = ceil_div(n_tokens, B);
+  if (nblk > p->desc.max_blocks_per_seq) return PKV_ERR_CAPACITY;
+  if (injected_failure(p)) return PKV_ERR_NO_BLOCKS;
+  // leading full blocks found in the cache
+  std::vector<int32_t> hits;
+  int64_t parent = -1;
+  PrefixKey key;
+  key.ns = ns;
+  for (int32_t i = 0; i < n_tokens / B; ++i) {
+    key.parent = parent;
+    key.tokens.assign(tokens + static_cast<int64_t>(i) * B, tokens + static_cast<int64_t>(i + 1) * B);
+    auto it = p->prefix_entries.find(key);
+    if (it == p->prefix_entries.end()) break;
+    hits.push_back(it->second.block);
+    parent = it->second.id;
+  }
+  const int64_t need = nblk - static_cast<int64_t>(hits.size());
+  if (need > static_cast<int64_t>(p->free_stack.size())) return PKV_ERR_NO_BLOCKS;
+  // commit
+  const int32_t seq = *p->free_ids.begin();
+  p->free_ids.erase(p->free_ids.begin());
+  p->live[seq] = 1;
+  std::vector<int32_t>& t = p->tables[seq];
+  t.clear();
+  for (int32_t blk : hits) {
+    if (p->refcount[blk] == 1) {  // was held by the cache alone: no longer evictable
+      p->evictable.erase(p->evictable_pos[blk]);
+      p->evictable_pos.erase(blk);
+    }
+    add_ref(p, blk);
+    t.push_back(blk);
+  }
+  for (int32_t i = static_cast<int32_t>(hits.size()); i < nblk; ++i) {
+    const int32_t blk = take_block(p);
+    t.push_back(blk);
+    if (static_cast<int64_t>(i + 1) * B <= n_tokens) {  // full block: register it
+      key.parent = parent;
+      key.tokens.assign(tokens + static_cast<int64_t>(i) * B, tokens + static_cast<int64_t>(i + 1) * B);
+      const int64_t id = p->next_entry_id++;
+      p->prefix_entries[key] = PrefixEntry{id, blk};
+      p->prefix_key_of_block[blk] = key;
+      add_ref(p, blk);  // the cache's own reference
+      parent = id;
+    }
+  }
+  p->lens[seq] = n_tokens;
+  p->n_tokens += n_tokens;
+  for (int32_t pos = 0; pos < n_tokens; ++pos) slots_out[pos] = static_cast<int64_t>(t[pos / B]) * B + pos % B;
+  *seq_out = seq;
+  *n_cached_out = static_cast<int32_t>(hits.size()) * B;
+  p->n_allocs_ok++;
+  return PKV_OK;
+}
+
+pkv_status pkv_prefix_evict(pkv_pool* p, int32_t max_blocks, int32_t* n_evicted_out) {
+  if (!p || max_blocks < 0) return PKV_ERR_INVALID;
+  int32_t n = 0;
+  while (n < max_blocks && !p->evictable.empty()) {
+    const int32_t blk = p->evictable.front();
+    p->evictable.pop_front();
+    p->evictable_pos.erase(blk);
+    auto kit = p->prefix_key_of_block.find(blk);
+    p->prefix_entries.erase(kit->second);
+    p->prefix_key_of_block.erase(kit);
+    if (drop_ref(p, blk)) p->free_stack.push_back(blk);
+    ++n;
+  }
+  if (n_evicted_out) *n_evicted_out = n;
+  return PKV_OK;
+}
+
+pkv_status pkv_prefix_stats(const pkv_pool* p, int32_t* n_cached_blocks, int32_t* n_evictable) {
+  if (!p) return PKV_ERR_INVALID;
+  if (n_cached_blocks) *n_cached_blocks = static_cast<int32_t>(p->prefix_entries.size());
+  if (n_evictable) *n_evictable = static_cast<int32_t>(p->evictable.size());
   return PKV_OK;
 }
 

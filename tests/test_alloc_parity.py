@@ -19,6 +19,8 @@ def same_state(lib: pkv.Pool, m: am.PoolModel):
         t, l = lib.block_table(live)
         mt, ml = m.block_table(live)
         assert t.tolist() == mt and l.tolist() == ml
+    if isinstance(m, am.PrefixCacheModel):
+        assert lib.prefix_stats() == m.prefix_stats()
     s = lib.stats()
     ms = m.stats()
     for k in ("num_free", "num_used", "num_shared", "num_cow", "num_seqs", "num_tokens"):
@@ -29,11 +31,20 @@ def drive(seed, NB, B, max_seqs, MB, n_ops, fail_after=-1, max_append=40):
     rng = np.random.default_rng(seed)
     perm = rng.permutation(NB)
     lib = pkv.Pool(1, 2, 64, B, NB, max_seqs, MB, pkv.F32, initial_free_list=perm, fail_after_n_allocs=fail_after)
-    m = am.PoolModel(NB, B, max_seqs, MB, initial_free_list=perm, fail_after_n_allocs=fail_after)
+    m = am.PrefixCacheModel(NB, B, max_seqs, MB, initial_free_list=perm, fail_after_n_allocs=fail_after)
     for _ in range(n_ops):
         live = sorted(m.tables)
         r = rng.random()
-        if r < 0.2 or not live:
+        if r < 0.08:
+            ns = int(rng.integers(0, 2))
+            toks = [int(x) for x in rng.integers(0, 2, size=int(rng.integers(0, 3 * B + 5)))]
+            a = lib.alloc_prefix_raw(ns, toks)
+            b = m.alloc_prefix(ns, toks)
+            assert a[0] == b[0] and a[1] == b[1] and a[2].tolist() == b[2] and a[3] == b[3]
+        elif r < 0.1:
+            k = int(rng.integers(0, 4))
+            assert lib.prefix_evict(k) == m.evict(k)
+        elif r < 0.2 or not live:
             n = int(rng.integers(0, max_append))
             a = lib.alloc_raw(-1, n)
             b = m.alloc(-1, n)

@@ -11,6 +11,7 @@ import torch
 
 import paged_kv_cache_494_b300 as pkv
 import synth
+from oracle import native
 from tests.gpu_cases import TOL, Case, case_from_workload, to_device
 
 pytestmark = pytest.mark.gpu
@@ -183,4 +184,53 @@ def test_window_with_released_blocks(path):
     for _ in range(20):
         c.decode_step_append()
     check(c, c.gpu_decode(0, window=W), c.oracle_decode(window=W))
+    assert pkv.last_error() == pkv.OK
+
+
+def test_prefix_cache_requests_decode(path):
+    """Requests built through the prefix cache share a 200-token system prompt's full blocks. Each
+    caller writes K/V only for positions the cache did not already hold; decode must match the oracle
+    (which built its own tables with the cache model and scattered the same values on the host)."""
+    from oracle import alloc_model as am
+    from oracle import cache_ops as ocache
+    from tests.gpu_cases import to_device
+    B, Hkv, Hq, D, NB = 16, 8, 32, 128, 300
+    fl = synth.free_list(NB, 9)
+    pool = pkv.Pool(1, Hkv, D, B, NB, 16, 64, pkv.BF16, initial_free_list=fl)
+    model = am.PrefixCacheModel(NB, B, 16, 64, initial_free_list=fl)
+    kc = torch.full((NB, Hkv, B, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    hk = np.full((NB, Hkv, B, D), synth.nan_bits("bf16"), dtype=np.uint16)
+    hv = np.full_like(hk, synth.nan_bits("bf16"))
+    system = list(range(200))
+    sys_kv = synth.normal_f32((2, 200, Hkv, D), 9, 1)       # K/V of the shared prompt positions
+    seqs = []
+    for r in range(6):
+        suffix_len = [0, 3, 40, 1, 77, 120][r]
+        toks = system + [1000 + 10 * r + i for i in range(suffix_len)]
+        suf_kv = synth.normal_f32((2, suffix_len, Hkv, D), 9, 10 + r)
+        kv = np.concatenate([sys_kv, suf_kv], axis=1)
+        sid, slots, ncached = pool.alloc_prefix(3, toks)
+        st, msid, mslots, mncached = model.alloc_prefix(3, toks)
+        assert st == 0 and (msid, mslots, mncached) == (sid, slots.tolist(), ncached)
+        assert ncached == (0 if r == 0 else 192)
+        k = synth.encode(kv[0, ncached:], "bf16")
+        v = synth.encode(kv[1, ncached:], "bf16")
+        w_slots = torch.from_numpy(slots[ncached:].copy()).cuda()
+        pool.reshape_and_cache(to_device(k, "bf16"), to_device(v, "bf16"), w_slots, kc, vc)
+        ocache.reshape_and_cache(hk, hv, k, v, mslots[ncached:])
+        seqs.append(sid)
+    assert pool.prefix_stats() == model.prefix_stats()
+    tables, lens = pool.block_table(seqs)
+    mtab, mlens = model.block_table(seqs)
+    assert tables.tolist() == mtab
+    q_stored = synth.encode(synth.normal_f32((6, Hq, D), 9, 99), "bf16")
+    out = torch.empty(6, Hq, D, device="cuda")
+    ws = torch.empty(pool.decode_workspace_bytes(6, Hq) // 4 + 4, device="cuda")
+    pool.paged_decode(out, to_device(q_stored, "bf16"), kc, vc, torch.from_numpy(tables).cuda(),
+                      torch.from_numpy(lens).cuda(), 1 / math.sqrt(D), workspace=ws)
+    ref = native.decode(q_stored, hk, hv, np.asarray(mtab, dtype=np.int32), np.asarray(mlens, dtype=np.int32),
+                        1 / math.sqrt(D))
+    err = float(np.max(np.abs(out.double().cpu().numpy() - ref)))
+    assert err <= 2e-3, err
     assert pkv.last_error() == pkv.OK
