@@ -94,6 +94,39 @@ def paged_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables
     return out
 
 
+def paged_prefill(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables: np.ndarray,
+                  lens: Sequence[int], cu_q: Sequence[int], scale: float, window: int = 0) -> np.ndarray:
+    """Causal attention of the last q_len_b positions of each sequence over its paged context.
+
+    Reading of the pages: prefill and generation are separate phases of the same request
+    ("¿Cuánta memoria reservar para la caché KV?", "Verificar una carga representativa por
+    etapas"; "Servicio de modelos..." §7: prefill work and decode steps have different shapes).
+    A prefill (or multi-token append) adds q_len_b positions to a sequence of final length len_b;
+    query i (rows cu_q[b] + i of q) sits at position p = len_b - q_len_b + i and, as in any causal
+    decoder, attends to positions [0, p] (or [max(0, p - window + 1), p] with a sliding window).
+    q: [total_q, Hq, D]; returns [total_q, Hq, D] binary64. With q_len_b = 1 this is decode.
+    """
+    total, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    qd = to_f64(q)
+    out = np.zeros((total, Hq, D), dtype=np.float64)
+    for b in range(len(lens)):
+        L = int(lens[b])
+        q0, q1 = int(cu_q[b]), int(cu_q[b + 1])
+        if q1 == q0:
+            continue
+        for h in range(Hkv):
+            K = gather_sequence(k_cache, tables[b], L, h)
+            V = gather_sequence(v_cache, tables[b], L, h)
+            for i in range(q1 - q0):
+                p = L - (q1 - q0) + i
+                t0 = max(0, p - window + 1) if window > 0 else 0
+                for j in range(h * g, (h + 1) * g):
+                    out[q0 + i, j] = dense_attention(qd[q0 + i, j], K[t0:p + 1], V[t0:p + 1], scale)
+    return out
+
+
 def online_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float, block: int) -> np.ndarray:
     """The same operation as ``dense_attention`` via the running max/sum recurrence over blocks.
 

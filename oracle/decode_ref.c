@@ -100,3 +100,69 @@ int oracle_decode(double* out, const void* q, int q_dtype, const void* k_cache, 
   }
   return used;
 }
+
+/* Causal prefill / multi-token append (same definition, one query row per new position):
+ * sequence b has final length lens[b] and its last q_len_b = cu_q[b+1] - cu_q[b] positions are
+ * queries; query i (row cu_q[b] + i of q, position p = lens[b] - q_len_b + i) attends to positions
+ * [max(0, p - window + 1), p] (window <= 0: [0, p]). q: [total_q][Hq][D]; out: [total_q][Hq][D].
+ * Reading of the pages: prefill and generation are separate phases of one request ("¿Cuánta memoria
+ * reservar para la caché KV?", "Verificar una carga representativa por etapas"). */
+int oracle_prefill(double* out, const void* q, int q_dtype, const void* k_cache, const void* v_cache, int kv_dtype,
+                   const int32_t* tables, const int32_t* lens, const int32_t* cu_q, int n_seqs, int num_q_heads,
+                   int num_kv_heads, int head_dim, int block_size, int max_blocks, double scale, int window,
+                   int n_threads) {
+  if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0) return -1;
+  const int g = num_q_heads / num_kv_heads;
+  const int D = head_dim;
+  const long total = (long)cu_q[n_seqs] * num_q_heads;
+  if (n_threads <= 0) n_threads = omp_get_max_threads();
+  int used = 1;
+#pragma omp parallel num_threads(n_threads)
+  {
+#pragma omp single
+    used = omp_get_num_threads();
+#pragma omp for schedule(dynamic, 4)
+    for (long r = 0; r < total; ++r) {
+      const long row = r / num_q_heads;
+      const int j = (int)(r % num_q_heads);
+      const int h = j / g;
+      int b = 0;
+      while (cu_q[b + 1] <= row) ++b;
+      const int qlen = cu_q[b + 1] - cu_q[b];
+      const int p = lens[b] - qlen + (int)(row - cu_q[b]);
+      const int t0 = (window > 0 && p - window + 1 > 0) ? p - window + 1 : 0;
+      const int L = p + 1 - t0;
+      double* o = out + r * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      if (L <= 0) continue;
+      double* s = (double*)malloc(sizeof(double) * (size_t)L);
+      double* qv = (double*)malloc(sizeof(double) * (size_t)D);
+      for (int d = 0; d < D; ++d) qv[d] = load_value(q, q_dtype, ((size_t)row * num_q_heads + j) * D + d);
+      double m = -INFINITY;
+      for (int t = 0; t < L; ++t) {
+        const int pos = t0 + t;
+        const long blk = tables[(long)b * max_blocks + pos / block_size];
+        const size_t base = (((size_t)blk * num_kv_heads + h) * block_size + (pos % block_size)) * D;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d) acc += load_value(k_cache, kv_dtype, base + d) * qv[d];
+        s[t] = scale * acc;
+        if (s[t] > m) m = s[t];
+      }
+      double l = 0.0;
+      for (int t = 0; t < L; ++t) {
+        s[t] = exp(s[t] - m);
+        l += s[t];
+      }
+      for (int t = 0; t < L; ++t) {
+        const int pos = t0 + t;
+        const long blk = tables[(long)b * max_blocks + pos / block_size];
+        const size_t base = (((size_t)blk * num_kv_heads + h) * block_size + (pos % block_size)) * D;
+        for (int d = 0; d < D; ++d) o[d] += s[t] * load_value(v_cache, kv_dtype, base + d);
+      }
+      for (int d = 0; d < D; ++d) o[d] /= l;
+      free(s);
+      free(qv);
+    }
+  }
+  return used;
+}

@@ -37,6 +37,12 @@ def _load():
                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                       ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+        f2 = _lib.oracle_prefill
+        f2.restype = ctypes.c_int
+        f2.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                       ctypes.c_int]
     return _lib
 
 
@@ -76,6 +82,28 @@ def decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables: np.n
         raise ValueError("oracle_decode rejected its arguments")
     res = out.reshape(n, Hq, D) if rows_arr is None else out
     return (res, used) if return_threads else res
+
+
+def prefill(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables: np.ndarray, lens: np.ndarray,
+            cu_q: np.ndarray, scale: float, window: int = 0, n_threads: int = 0) -> np.ndarray:
+    """Binary64 causal prefill over pages (see oracle_prefill in decode_ref.c). q [total_q, Hq, D]."""
+    lib = _load()
+    q = np.ascontiguousarray(q)
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    tables = np.ascontiguousarray(tables, dtype=np.int32)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    cu_q = np.ascontiguousarray(cu_q, dtype=np.int32)
+    total, Hq, D = q.shape
+    _, Hkv, B, _ = k_cache.shape
+    out = np.zeros((total, Hq, D), dtype=np.float64)
+    used = lib.oracle_prefill(out.ctypes.data, q.ctypes.data, _dtype_code(q), k_cache.ctypes.data,
+                              v_cache.ctypes.data, _dtype_code(k_cache), tables.ctypes.data, lens.ctypes.data,
+                              cu_q.ctypes.data, lens.size, Hq, Hkv, D, B, tables.shape[1], float(scale), int(window),
+                              int(n_threads))
+    if used < 0:
+        raise ValueError("oracle_prefill rejected its arguments")
+    return out
 
 
 def decode_fn_from(lib_path: str):
