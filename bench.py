@@ -510,6 +510,59 @@ def bench_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def bench_prefill(args):
+    """Causal paged prefill (prefill_bf16): every position of 16 x 2,048-token prompts is a query.
+    Reports useful attention TFLOP/s (4 * D per (query row, attended key): q.K and p.V) against the
+    measured dense bf16 tensor peak, and KV bytes per launch."""
+    import torch
+    import paged_kv_cache_494_b300 as pkv
+    w = synth.workload("prefill_bf16")
+    lens = synth.lengths(w, args.seed)
+    NB = synth.pool_blocks(w, lens)
+    MB = -(-int(lens.max()) // w.block_size)
+    pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs, MB, pkv.BF16,
+                    initial_free_list=synth.free_list(NB, args.seed))
+    seqs = [pool.alloc(-1, int(t))[0] for t in lens]
+    tables, l = pool.block_table(seqs)
+    g = torch.Generator(device="cuda").manual_seed(args.seed)
+    shape = (NB, w.num_kv_heads, w.block_size, w.head_dim)
+    kc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
+    vc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
+    total = int(lens.sum())
+    q = torch.randn(total, w.num_q_heads, w.head_dim, device="cuda", dtype=torch.bfloat16, generator=g)
+    out = torch.empty(total, w.num_q_heads, w.head_dim, device="cuda")
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
+    t_tab, t_len = torch.from_numpy(tables).cuda(), torch.from_numpy(l).cuda()
+    for _ in range(args.warmup):
+        pool.paged_prefill(out, q, kc, vc, t_tab, t_len, cu, w.scale)
+    torch.cuda.synchronize()
+    Ev = lambda: torch.cuda.Event(enable_timing=True)
+    a, b = Ev(), Ev()
+    with ClockSampler(0) as clocks:
+        a.record()
+        for _ in range(args.steps):
+            pool.paged_prefill(out, q, kc, vc, t_tab, t_len, cu, w.scale)
+        b.record()
+        torch.cuda.synchronize()
+    assert pkv.last_error() == pkv.OK
+    t = a.elapsed_time(b) / args.steps * 1e-3
+    keys = sum(int(L) * (int(L) + 1) // 2 for L in lens)          # attended (row, key) pairs per head
+    flops = 4.0 * w.head_dim * keys * w.num_q_heads
+    kv_bytes = int(lens.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peak = float(json.load(f)["bf16_tflops"])
+    tf = flops / t / 1e12
+    print(json.dumps({
+        "metric": "paged-prefill causal attention TFLOP/s (useful FLOPs)", "value": round(tf, 2), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 4),
+        "higher_is_better": True, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
+        "config": {"workload": "prefill_bf16", "description": w.description},
+        "kv_gb_per_s": round(kv_bytes / t / 1e9, 1),
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tf / peak, 4), "note": "mma.sync m16n8k16; P carried as bf16 hi + lo (2 mmas)"},
+        "clocks": clocks.summary()}), flush=True)
+
+
 def profile_decode(args):
     """Small case for ncu: one layer of the workload (about 0.8 GB of KV, above L2), decode x5."""
     import torch
@@ -547,11 +600,15 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=[WORKLOAD, "prefill_bf16"], default=WORKLOAD,
+                    help="serve256_bf16 (the benchmark line) or prefill_bf16 (causal prefill kernel line)")
     ap.add_argument("--profile-decode", action="store_true",
                     help="run one layer's decode 5 times (small case for ncu); prints no bench line")
     args = ap.parse_args(argv)
     if args.profile_decode:
         return profile_decode(args)
+    if args.workload == "prefill_bf16":
+        return bench_prefill(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()

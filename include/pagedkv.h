@@ -241,6 +241,22 @@ PKV_API pkv_status pkv_paged_decode_window(const pkv_pool* pool, float* out, con
                                            float scale, int32_t window, int32_t partition_tokens, void* workspace,
                                            size_t workspace_bytes, void* stream);
 
+/* Causal paged prefill / multi-token append attention. Sequence b has final length len_b =
+ * context_lens[b] (its new positions included) and its last q_len_b = cu_q[b+1] - cu_q[b] positions
+ * are queries: row cu_q[b] + i of q is position p = len_b - q_len_b + i, and for each query head j
+ *     out[row][j][:] = sum_{t in T(p)} softmax_t(scale * q[row][j] . K_b[t]) V_b[t]
+ * with T(p) = [0, p], or [max(0, p - window + 1), p] when window > 0 (prefill and generation are
+ * separate phases of one request: "¿Cuánta memoria reservar para la caché KV?", "Verificar una carga
+ * representativa por etapas"; exact attention: "Servicio de modelos…" §6). The K/V of the new
+ * positions must already be in the cache (pkv_reshape_and_cache, same stream). q_len_b = 1 for all b
+ * is a decode step. q: [total_q][num_q_heads][D] bf16, out: float32 same shape; cu_q: device int32
+ * [n_seqs + 1], cu_q[0] = 0, cu_q[n_seqs] = total_q, q_len_b <= len_b. Needs a bf16 pool (D 64 or 128,
+ * block size a multiple of 16, max_blocks_per_seq <= 8192) and num_q_heads / Hkv <= 8. No workspace. */
+PKV_API pkv_status pkv_paged_prefill(const pkv_pool* pool, float* out, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+                                     const int32_t* cu_q, int32_t n_seqs, int32_t total_q, int32_t num_q_heads,
+                                     float scale, int32_t window, void* stream);
+
 /* Workspace bytes pkv_paged_decode needs for these arguments on the current device. */
 PKV_API size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t n_seqs, int32_t num_q_heads,
                                   int32_t partition_tokens);

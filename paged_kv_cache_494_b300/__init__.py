@@ -75,6 +75,8 @@ _SIGS = {
     "pkv_paged_decode_window": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
                                                _i32, _i32, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
+    "pkv_paged_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
+                                         _i32, _vp]),
     "pkv_paged_decode_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32,
                                                _vp]),
     "pkv_last_error": (ctypes.c_int, [_vp]),
@@ -318,6 +320,15 @@ class Pool:
         _check(lib.pkv_paged_decode(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache), _dev(block_tables),
                                     _dev(context_lens), n_seqs, num_q_heads, float(scale), int(partition_tokens),
                                     _dev(workspace), ws_bytes, _stream(stream)), "pkv_paged_decode")
+
+    def paged_prefill(self, out, q, k_cache, v_cache, block_tables, context_lens, cu_q, scale: float,
+                      window: int = 0, stream=None) -> None:
+        """pkv_paged_prefill: causal attention of the last q_len_b positions of each sequence."""
+        n_seqs = int(context_lens.shape[0])
+        total_q, num_q_heads = int(q.shape[0]), int(q.shape[1])
+        _check(lib.pkv_paged_prefill(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache), _dev(block_tables),
+                                     _dev(context_lens), _dev(cu_q), n_seqs, total_q, num_q_heads, float(scale),
+                                     int(window), _stream(stream)), "pkv_paged_prefill")
 
     def paged_decode_static(self, out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                             partition_tokens: int = 0, stream=None) -> None:

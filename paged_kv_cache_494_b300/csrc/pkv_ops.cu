@@ -16,6 +16,7 @@
 
 #include "kernels_cache.cuh"
 #include "kernels_decode.cuh"
+#include "kernels_prefill.cuh"
 #include "pkv_pool.hpp"
 
 namespace {
@@ -284,6 +285,71 @@ pkv_status pkv_copy_blocks(const pkv_pool* p, void* const* k_caches, void* const
                                static_cast<cudaStream_t>(stream), lc, pairs, d.num_layers, block_bytes / 16,
                                d.num_blocks);
   return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens, const int32_t* cu_q,
+                             int32_t n_seqs, int32_t total_q, int32_t num_q_heads, float scale, int32_t window,
+                             void* stream) {
+  if (!p || n_seqs < 0 || total_q < 0 || window < 0) return PKV_ERR_INVALID;
+  if (n_seqs == 0 || total_q == 0) return PKV_OK;
+  const pkv_pool_desc& d = p->desc;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !cu_q) return PKV_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cu_q) & 3u))
+    return PKV_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID;
+  if (d.dtype != PKV_BF16 || (d.head_dim != 64 && d.head_dim != 128) || d.block_size % pkv_dev::kChunk != 0)
+    return PKV_ERR_INVALID;
+  if (num_q_heads <= 0 || num_q_heads % d.num_kv_heads != 0) return PKV_ERR_INVALID;
+  if (n_seqs > 16384 || d.max_blocks_per_seq > 8192) return PKV_ERR_INVALID;
+  const int g = num_q_heads / d.num_kv_heads;
+  using PK = void (*)(pkv_dev::PrefillArgs, pkv_dev::TmaMaps);
+  PK kern = nullptr;
+  int tq = 0, stage_bytes = 0;
+#define PKV_PREFILL_CASE(DD, GG)                                       \
+  if (d.head_dim == DD && g == GG) {                                   \
+    kern = pkv_dev::paged_prefill_kernel<DD, GG>;                      \
+    tq = pkv_dev::PrefillShape<DD, GG>::TQ;                            \
+    stage_bytes = pkv_dev::PrefillShape<DD, GG>::kStageBytes;          \
+  }
+  PKV_PREFILL_CASE(64, 1) PKV_PREFILL_CASE(64, 2) PKV_PREFILL_CASE(64, 3) PKV_PREFILL_CASE(64, 4)
+  PKV_PREFILL_CASE(64, 5) PKV_PREFILL_CASE(64, 6) PKV_PREFILL_CASE(64, 7) PKV_PREFILL_CASE(64, 8)
+  PKV_PREFILL_CASE(128, 1) PKV_PREFILL_CASE(128, 2) PKV_PREFILL_CASE(128, 3) PKV_PREFILL_CASE(128, 4)
+  PKV_PREFILL_CASE(128, 5) PKV_PREFILL_CASE(128, 6) PKV_PREFILL_CASE(128, 7) PKV_PREFILL_CASE(128, 8)
+#undef PKV_PREFILL_CASE
+  if (!kern) return PKV_ERR_INVALID;
+  const int stages = env_int("PKV_PREFILL_STAGES", 4);
+  const size_t smem = pkv_dev::prefill_smem_bytes(stages, stage_bytes, n_seqs, d.max_blocks_per_seq);
+  if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return PKV_ERR_CUDA;
+  const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size;
+  if (rows > 0x7fffffffLL) return PKV_ERR_INVALID;
+  pkv_dev::TmaMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d)) return PKV_ERR_CUDA;
+  pkv_dev::PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.cu_q = cu_q;
+  a.n_seqs = n_seqs;
+  a.Hq = num_q_heads;
+  a.Hkv = d.num_kv_heads;
+  a.B = d.block_size;
+  a.NB = d.num_blocks;
+  a.MB = d.max_blocks_per_seq;
+  a.window = window;
+  a.stages = stages;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int64_t tiles_ub = (static_cast<int64_t>(total_q) + tq - 1) / tq + n_seqs;   // >= sum of tiles
+  if (tiles_ub > 0x7fffffffLL || d.num_kv_heads > 65535) return PKV_ERR_INVALID;
+  if (launch(kern, dim3(static_cast<unsigned>(tiles_ub), d.num_kv_heads), dim3(128), smem,
+             static_cast<cudaStream_t>(stream), a, maps) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
 }
 
 size_t pkv_decode_workspace_bytes(const pkv_pool* p, int32_t n_seqs, int32_t num_q_heads, int32_t partition_tokens) {

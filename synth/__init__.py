@@ -99,6 +99,12 @@ WORKLOADS: Dict[str, Workload] = {
                     "block), so the first append of each child copies the shared partial block",
         n_layers=1, n_seqs=128, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
         dtype="bf16", length_kind="prefix", length_args=(1016, 0, 512), pool_rule="(pages)*1.1"),
+    "prefill_bf16": Workload(
+        name="prefill_bf16",
+        description="paged prefill (causal), bf16: 16 prompts of 2,048 tokens written to the pool, every "
+                    "position a query, 32 q / 8 kv heads, head_dim 128, block 16",
+        n_layers=1, n_seqs=16, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+        dtype="bf16", length_kind="fixed", length_args=(2048,) * 16, pool_rule="pages*1.1"),
     "long_split_bf16": Workload(
         name="long_split_bf16",
         description="long-context split-KV decode, bf16: batch 8 x 32,768 tokens, 32 q / 8 kv heads, "
