@@ -16,7 +16,8 @@
  * Sliding window ("¿Cuánta memoria reservar para la caché KV?", "Adaptar el presupuesto a la
  * estrategia de caché"): with window > 0 only positions [max(0, len - window), len) are attended to.
  *
- * Storage types: 0 = float32, 1 = bfloat16 bit patterns (decoded exactly).
+ * Storage types: 0 = float32, 1 = bfloat16 bit patterns (decoded exactly), 3 = binary64 (e.g. a
+ * dequantised fp8 pool).
  * Cache layout: cache[block][kv_head][offset][dim].
  */
 #include <math.h>
@@ -27,6 +28,7 @@
 
 static double load_value(const void* base, int dtype, size_t idx) {
   if (dtype == 0) return (double)((const float*)base)[idx];
+  if (dtype == 3) return ((const double*)base)[idx];
   uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
   float f;
   memcpy(&f, &bits, sizeof f);

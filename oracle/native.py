@@ -51,6 +51,8 @@ def _dtype_code(a: np.ndarray) -> int:
         return 0
     if a.dtype == np.uint16:
         return 1
+    if a.dtype == np.float64:
+        return 3
     raise TypeError(f"oracle stores float32 or bf16 bits (uint16), got {a.dtype}")
 
 
