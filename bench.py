@@ -184,26 +184,38 @@ def kernel_sha() -> str:
 class Serve:
     """Pool, caches and per-step inputs of the serving workload on one GPU."""
 
-    def __init__(self, seed: int, n_steps: int, device):
+    def __init__(self, seed: int, n_steps: int, device, fp8: bool = False):
         import torch
         import paged_kv_cache_494_b300 as pkv
         self.torch, self.pkv = torch, pkv
         w = synth.workload(WORKLOAD)
         self.w = w
+        self.fp8 = fp8
         self.L, self.n, self.Hq, self.Hkv, self.D, self.B = (w.n_layers, w.n_seqs, w.num_q_heads, w.num_kv_heads,
                                                              w.head_dim, w.block_size)
         self.lens0 = synth.lengths(w, seed)
         NB = synth.pool_blocks(w, self.lens0 + n_steps)
         self.MB = -(-(int(self.lens0.max()) + n_steps) // self.B) + 1
-        self.pool = pkv.Pool(self.L, self.Hkv, self.D, self.B, NB, self.n + 1, self.MB, pkv.BF16,
+        self.pool = pkv.Pool(self.L, self.Hkv, self.D, self.B, NB, self.n + 1, self.MB, pkv.FP8 if fp8 else pkv.BF16,
                              initial_free_list=synth.free_list(NB, seed))
         self.seqs = [self.pool.alloc(-1, int(t))[0] for t in self.lens0]
         self.device = device
         g = torch.Generator(device=device).manual_seed(seed)
         shape = (NB, self.Hkv, self.B, self.D)
         # prefilled context: random K/V everywhere (values are data; only their bytes matter here)
-        self.k_caches = [torch.randn(shape, device=device, dtype=torch.bfloat16, generator=g) for _ in range(self.L)]
-        self.v_caches = [torch.randn(shape, device=device, dtype=torch.bfloat16, generator=g) for _ in range(self.L)]
+        if fp8:
+            kshape, vshape, sshape = self.pool.fp8_shapes()
+            self.k_caches = [torch.randint(0, 0x7E, kshape, device=device, dtype=torch.uint8, generator=g)
+                             for _ in range(self.L)]
+            self.v_caches = [torch.randint(0, 0x7E, vshape, device=device, dtype=torch.uint8, generator=g)
+                             for _ in range(self.L)]
+            self.k_scales = [torch.rand(sshape, device=device, generator=g) * 0.01 for _ in range(self.L)]
+            self.v_scales = [torch.rand(sshape, device=device, generator=g) * 0.01 for _ in range(self.L)]
+        else:
+            self.k_caches = [torch.randn(shape, device=device, dtype=torch.bfloat16, generator=g)
+                             for _ in range(self.L)]
+            self.v_caches = [torch.randn(shape, device=device, dtype=torch.bfloat16, generator=g)
+                             for _ in range(self.L)]
         self.q = [torch.randn(self.n, self.Hq, self.D, device=device, dtype=torch.bfloat16, generator=g)
                   for _ in range(self.L)]
         self.k_new = [torch.randn(self.n, self.Hkv, self.D, device=device, dtype=torch.bfloat16, generator=g)
@@ -227,19 +239,30 @@ class Serve:
         return steps
 
     def kv_bytes(self, lens: np.ndarray) -> int:
-        return int(lens.sum()) * self.Hkv * self.D * 2 * 2 * self.L
+        per_token_head = (self.D + 4) * 2 if self.fp8 else self.D * 2 * 2   # K + V (+ fp8 scales)
+        return int(lens.sum()) * self.Hkv * per_token_head * self.L
 
     def run_step(self, step, dec_events=None) -> int:
         """Enqueue one step: per layer K1 then decode. Returns the number of kernels launched."""
         slots, tables, lens, _ = step
         scale = self.w.scale
         for l in range(self.L):
-            self.pool.reshape_and_cache(self.k_new[l], self.v_new[l], slots, self.k_caches[l], self.v_caches[l],
-                                        stream=self.stream)
+            if self.fp8:
+                self.pool.reshape_and_cache_fp8(self.k_new[l], self.v_new[l], slots, self.k_caches[l],
+                                                self.v_caches[l], self.k_scales[l], self.v_scales[l],
+                                                stream=self.stream)
+            else:
+                self.pool.reshape_and_cache(self.k_new[l], self.v_new[l], slots, self.k_caches[l], self.v_caches[l],
+                                            stream=self.stream)
             if dec_events is not None:
                 dec_events[l][0].record(self.stream)
-            self.pool.paged_decode(self.out[l], self.q[l], self.k_caches[l], self.v_caches[l], tables, lens, scale,
-                                   0, self.ws, stream=self.stream)
+            if self.fp8:
+                self.pool.paged_decode_fp8(self.out[l], self.q[l], self.k_caches[l], self.v_caches[l],
+                                           self.k_scales[l], self.v_scales[l], tables, lens, scale, 0, 0, self.ws,
+                                           stream=self.stream)
+            else:
+                self.pool.paged_decode(self.out[l], self.q[l], self.k_caches[l], self.v_caches[l], tables, lens,
+                                       scale, 0, self.ws, stream=self.stream)
             if dec_events is not None:
                 dec_events[l][1].record(self.stream)
         return self.L * 3
@@ -251,7 +274,8 @@ def bench_cuda(args, world, rank, local):
     torch.cuda.set_device(device)
     dist = init_dist(world, "nccl")
     steps_total = args.warmup + 2 * args.steps
-    s = Serve(args.seed + rank, 2 * steps_total + args.warmup + args.steps + 4, device)
+    fp8 = args.workload == "serve256_fp8"
+    s = Serve(args.seed + rank, 2 * steps_total + args.warmup + args.steps + 4, device, fp8=fp8)
     pkv = s.pkv
     plan = s.plan_steps(steps_total)
     Ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -297,7 +321,7 @@ def bench_cuda(args, world, rank, local):
     achieved = dec_bytes_per_launch / (float(np.mean(dec_ms)) * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
 
-    e2e = bench_e2e(s, args, dist, device)
+    e2e = bench_e2e(s, args, dist, device) if not fp8 else None
     traffic = decode_traffic_record()
     clk = clocks.summary()
     line = {
@@ -311,11 +335,13 @@ def bench_cuda(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "fp8e4m3" if fp8 else "bf16",
         "accumulate": "f32",
         "data": "synthetic",
         "config": {
-            "workload": WORKLOAD, "description": synth.workload(WORKLOAD).description,
+            "workload": args.workload,
+            "description": synth.workload(WORKLOAD).description + (
+                "; fp8 E4M3 pool with per-(token, head) scales (KV bytes = codes + scales)" if fp8 else ""),
             "n_seqs": s.n, "layers": s.L, "num_q_heads": s.Hq, "num_kv_heads": s.Hkv, "head_dim": s.D,
             "block_size": s.B, "mean_context": float(np.mean(plan[args.warmup][3])),
             "kv_gb_per_step": round(kv_bytes / args.steps / 1e9, 3),
@@ -337,7 +363,11 @@ def bench_cuda(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if fp8:
+        line["metric"] = "paged-decode KV GB/s read (fp8 pool, codes + scales); decode seq-steps/sec"
+        line.pop("e2e")
+        line["roofline"]["traffic"] = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         line["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -600,8 +630,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=[WORKLOAD, "prefill_bf16"], default=WORKLOAD,
-                    help="serve256_bf16 (the benchmark line) or prefill_bf16 (causal prefill kernel line)")
+    ap.add_argument("--workload", choices=[WORKLOAD, "serve256_fp8", "prefill_bf16"], default=WORKLOAD,
+                    help="serve256_bf16 (the benchmark line), serve256_fp8 (the same step on an fp8 pool) or "
+                         "prefill_bf16 (causal prefill kernel line)")
     ap.add_argument("--profile-decode", action="store_true",
                     help="run one layer's decode 5 times (small case for ncu); prints no bench line")
     args = ap.parse_args(argv)

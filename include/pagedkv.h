@@ -65,7 +65,13 @@ typedef enum {
   PKV_ERR_SCRATCH_TOO_SMALL = -8 /* pkv_paged_decode_static: the call needs more than the built-in scratch */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* Storage type of a pool. PKV_FP8: K and V as FP8 E4M3 codes with one float32 scale per (token,
+ * KV head) for K and one for V; q stays bf16. FP8 layouts: k_cache [NB][Hkv][B][D] codes (token-major
+ * like the others), v_cache [NB][Hkv][D][B] codes (dim-major within a page), k_scale / v_scale
+ * [NB][Hkv][B] float32. Quantising the cache is one of the cache strategies ("¿Cuánta memoria reservar
+ * para la caché KV?", "Adaptar el presupuesto a la estrategia de caché"); it changes the numerics, so
+ * fp8 pools use the *_fp8 entry points and their own contract. */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_FP8 = 2 } pkv_dtype;
 
 typedef struct {
   int32_t num_layers;          /* layers sharing the block table (>= 1) */
@@ -106,10 +112,13 @@ PKV_API pkv_status pkv_pool_create(const pkv_pool_desc* desc, pkv_pool** out);
 PKV_API void pkv_pool_destroy(pkv_pool* pool);
 
 /* Bytes of K plus V per token across all layers: 2 * L * Hkv * D * sizeof(dtype)
- * ("Servicio de modelos de lenguaje con un presupuesto de memoria" §3). */
+ * ("Servicio de modelos de lenguaje con un presupuesto de memoria" §3); fp8 pools add their scales,
+ * 2 * L * Hkv * 4 bytes. */
 PKV_API int64_t pkv_bytes_per_token(const pkv_pool* pool);
 /* Bytes of ONE cache tensor (K or V) of ONE layer: NB * Hkv * B * D * sizeof(dtype). */
 PKV_API int64_t pkv_layer_cache_bytes(const pkv_pool* pool);
+/* fp8 pools: bytes of ONE scale tensor (k_scale or v_scale) of ONE layer, NB * Hkv * B * 4; else 0. */
+PKV_API int64_t pkv_layer_scale_bytes(const pkv_pool* pool);
 
 /* ---- allocator (host only, no device work, all-or-nothing) ---------------------------------- */
 
@@ -228,6 +237,33 @@ PKV_API pkv_status pkv_paged_decode(const pkv_pool* pool, float* out, const void
                             const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                             int32_t n_seqs, int32_t num_q_heads, float scale, int32_t partition_tokens,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- fp8 pools ------------------------------------------------------------------------------- */
+
+/* Quantising slot-mapped append into an fp8 pool: for each token i with slot s >= 0 and each KV head,
+ * the row x = k[i][h][:] (bf16) is stored as codes e4m3(x / scale), rounded to nearest even and
+ * saturated to +-448, with scale = amax|x| / 448 (float32 IEEE division; 1 if amax == 0) written to
+ * k_scale[s/B][h][s%B]; the same for V into the dim-major v_cache. Deterministic and bit-reproducible. */
+PKV_API pkv_status pkv_reshape_and_cache_fp8(const pkv_pool* pool, const void* k, const void* v,
+                                             const int64_t* slots, int32_t n_tokens, void* k_cache, void* v_cache,
+                                             float* k_scale, float* v_scale, void* stream);
+
+/* Copy-on-write for fp8 pools: as pkv_copy_blocks, also copying the blocks' scales
+ * (k_scales / v_scales: HOST arrays of num_layers device pointers). */
+PKV_API pkv_status pkv_copy_blocks_fp8(const pkv_pool* pool, void* const* k_caches, void* const* v_caches,
+                                       void* const* k_scales, void* const* v_scales, const int32_t* pairs,
+                                       int32_t n_pairs, void* stream);
+
+/* Paged decode over an fp8 pool (head_dim 128, num_q_heads / Hkv <= 8): the attention of
+ * pkv_paged_decode_window over the dequantised values code * scale (q bf16, out float32), with the
+ * same split modes, window and workspace size. Contract: max abs error <= 2e-3 against the exact
+ * attention over the dequantised cache; |V| entries must stay below ~7000 (f16 range of the scaled
+ * softmax weights). */
+PKV_API pkv_status pkv_paged_decode_fp8(const pkv_pool* pool, float* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const float* k_scale, const float* v_scale,
+                                        const int32_t* block_tables, const int32_t* context_lens, int32_t n_seqs,
+                                        int32_t num_q_heads, float scale, int32_t window, int32_t partition_tokens,
+                                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* Sliding-window variant: as pkv_paged_decode, but each query attends only to the last `window`
  * positions of its sequence, t in [max(0, len_b - window), len_b) ("¿Cuánta memoria reservar para la

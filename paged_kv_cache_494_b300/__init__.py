@@ -17,7 +17,7 @@ from typing import Iterable, List, Optional, Sequence, Tuple
 
 import numpy as np
 
-__all__ = ["Pool", "PagedKVError", "lib", "LIB_PATH", "F32", "BF16", "status_string", "last_error",
+__all__ = ["Pool", "PagedKVError", "lib", "LIB_PATH", "F32", "BF16", "FP8", "status_string", "last_error",
            "EXPORTED_SYMBOLS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +29,7 @@ if not os.path.exists(LIB_PATH):
 
 lib = ctypes.CDLL(LIB_PATH)
 
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2
 OK, ERR_INVALID, ERR_NO_BLOCKS, ERR_NO_SEQ, ERR_CUDA, ERR_DEVICE_BOUNDS, ERR_CAPACITY, ERR_DEVICE_TIMEOUT = (
     0, -1, -2, -3, -4, -5, -6, -7)
 ERR_SCRATCH_TOO_SMALL = -8
@@ -57,6 +57,7 @@ _SIGS = {
     "pkv_pool_destroy": (None, [_vp]),
     "pkv_bytes_per_token": (_i64, [_vp]),
     "pkv_layer_cache_bytes": (_i64, [_vp]),
+    "pkv_layer_scale_bytes": (_i64, [_vp]),
     "pkv_alloc": (ctypes.c_int, [_vp, _i32, _i32, _pi32, _pi64, _pi32, _pi32]),
     "pkv_append": (ctypes.c_int, [_vp, _pi32, _i32, _pi64, _pi32, _pi32]),
     "pkv_fork": (ctypes.c_int, [_vp, _i32, _pi32]),
@@ -75,6 +76,11 @@ _SIGS = {
     "pkv_paged_decode_window": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
                                                _i32, _i32, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
+    "pkv_reshape_and_cache_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "pkv_copy_blocks_fp8": (ctypes.c_int, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                           ctypes.POINTER(_vp), _vp, _i32, _vp]),
+    "pkv_paged_decode_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
+                                            _i32, _i32, _vp, _sz, _vp]),
     "pkv_paged_prefill": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
                                          _i32, _vp]),
     "pkv_paged_decode_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32,
@@ -177,8 +183,17 @@ class Pool:
     def layer_cache_bytes(self) -> int:
         return lib.pkv_layer_cache_bytes(self._h)
 
+    @property
+    def layer_scale_bytes(self) -> int:
+        return lib.pkv_layer_scale_bytes(self._h)
+
     def cache_shape(self) -> Tuple[int, int, int, int]:
         return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+
+    def fp8_shapes(self):
+        """fp8 pools: (k_cache [NB][Hkv][B][D], v_cache [NB][Hkv][D][B], scales [NB][Hkv][B]) shapes."""
+        NB, H, B, D = self.cache_shape()
+        return (NB, H, B, D), (NB, H, D, B), (NB, H, B)
 
     # -- allocator -----------------------------------------------------------------------------
     def alloc_raw(self, seq: int, n_tokens: int) -> Tuple[int, int, np.ndarray, List[Tuple[int, int]]]:
@@ -320,6 +335,28 @@ class Pool:
         _check(lib.pkv_paged_decode(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache), _dev(block_tables),
                                     _dev(context_lens), n_seqs, num_q_heads, float(scale), int(partition_tokens),
                                     _dev(workspace), ws_bytes, _stream(stream)), "pkv_paged_decode")
+
+    def reshape_and_cache_fp8(self, k, v, slots, k_cache, v_cache, k_scale, v_scale, stream=None) -> None:
+        n = int(slots.shape[0])
+        _check(lib.pkv_reshape_and_cache_fp8(self._h, _dev(k), _dev(v), _dev(slots), n, _dev(k_cache), _dev(v_cache),
+                                             _dev(k_scale), _dev(v_scale), _stream(stream)),
+               "pkv_reshape_and_cache_fp8")
+
+    def copy_blocks_fp8(self, k_caches, v_caches, k_scales, v_scales, pairs, stream=None) -> None:
+        L = self.num_layers
+        arr = lambda ts: (_vp * L)(*[_dev(t) for t in ts])
+        n = int(pairs.shape[0]) if pairs is not None else 0
+        _check(lib.pkv_copy_blocks_fp8(self._h, arr(k_caches), arr(v_caches), arr(k_scales), arr(v_scales),
+                                       _dev(pairs) if n else 0, n, _stream(stream)), "pkv_copy_blocks_fp8")
+
+    def paged_decode_fp8(self, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale: float,
+                         window: int = 0, partition_tokens: int = 0, workspace=None, stream=None) -> None:
+        n_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
+        ws_bytes = 0 if workspace is None else int(workspace.numel() * workspace.element_size())
+        _check(lib.pkv_paged_decode_fp8(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache), _dev(k_scale),
+                                        _dev(v_scale), _dev(block_tables), _dev(context_lens), n_seqs, num_q_heads,
+                                        float(scale), int(window), int(partition_tokens), _dev(workspace), ws_bytes,
+                                        _stream(stream)), "pkv_paged_decode_fp8")
 
     def paged_prefill(self, out, q, k_cache, v_cache, block_tables, context_lens, cu_q, scale: float,
                       window: int = 0, stream=None) -> None:

@@ -58,6 +58,8 @@ struct DecodeArgs {
   int32_t total_warps;           // warps of the decode grid (balanced-mode slot count / 2)
   int32_t window;                // > 0: attend only to the last `window` positions (sliding window)
   float scale_log2;              // scale * log2(e)
+  const float* k_scale;          // fp8 pools: [NB][Hkv][B] per-(token, head) scales (else unused)
+  const float* v_scale;
 };
 
 __device__ __forceinline__ int32_t clamped_len(const DecodeArgs& a, int32_t b) {
@@ -502,6 +504,165 @@ struct MmaMath {
     lt += __shfl_xor_sync(0xffffffffu, lt, 2);
     if (g >= G) return;
     const float inv = 1.f / lt;
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+      *reinterpret_cast<float2*>(dst + g * D + 8 * n + 2 * t) =
+          make_float2((r.o[n][0] + r.o[n][2]) * inv, (r.o[n][1] + r.o[n][3]) * inv);
+    if (ml != nullptr && t == 0) {
+      ml[2 * g] = r.m;
+      ml[2 * g + 1] = lt;
+    }
+  }
+};
+
+// ------------------------------------------------------------------------------------------------
+// FP8 E4M3 caches (D = 128), G <= 8: f16 tensor-core math on exactly converted codes.
+//
+// Stage: [K box: 16 rows x 128 B, 128-byte swizzle][V box: 128 dims x 16 tokens (V is stored
+// dim-major in fp8 pools)][16 K scales][16 V scales], padded to 5120 bytes.
+// q.K: the contraction over d is order-free, so within each 16-dim k-step lane t takes dims
+// 4t..4t+3 for both operands: ldmatrix on the fp8 rows hands each lane 4 consecutive codes, which
+// cvt turns into the two f16 pairs of its B fragment; q is loaded with the same dim order. The
+// n-tiles hold tokens {0,1,4,5,8,9,12,13} and {2,3,6,7,10,11,14,15}, so lane t's scores are tokens
+// 4t..4t+3 and its P fragment matches the V fragment ldmatrix reads from the dim-major V box
+// (tokens 4t..4t+3 of one dim). Per-token scales: S *= k_scale; P' = p * v_scale * 1024 is split
+// into f16 hi + lo (rows 0..7 / 8..15); the running max is raised when a chunk exceeds it by 2^2,
+// so p <= 4 and P' stays inside the f16 normal range for |V| < ~7000.
+// ------------------------------------------------------------------------------------------------
+template <int G>
+struct Fp8Math {
+  static_assert(G >= 1 && G <= 8, "G <= 8");
+  static constexpr int D = 128;
+  static constexpr int KBOX = kChunk * 128;
+  static constexpr int VBOX = D * kChunk;
+  static constexpr int kScaleOff = KBOX + VBOX;
+  static constexpr int kTxBytes = KBOX + VBOX + 2 * kChunk * 4;
+  static constexpr int kStageBytes = 5120;
+  static constexpr int KS = D / 16;
+  static constexpr int NT = D / 8;
+  static constexpr float kRescaleLog2 = 2.f;
+  static constexpr float kPScale = 1024.f;
+
+  struct Regs {
+    uint32_t qa[KS][2];
+    float o[NT][4];
+    float m, l;
+  };
+
+  __device__ static void issue(const DecodeArgs& a, const TmaMaps& maps, uint32_t dst, uint32_t bar, int64_t row0,
+                               uint64_t policy) {
+    const int64_t page = row0 / a.B;
+    const int32_t off = static_cast<int32_t>(row0 - page * a.B);
+    mbar_arrive_expect_tx(bar, kTxBytes);
+    tma_load_2d(dst, &maps.k, 0, static_cast<int32_t>(row0), bar, policy);
+    tma_load_2d(dst + KBOX, &maps.v, off, static_cast<int32_t>(page * D), bar, policy);
+    bulk_g2s_hint(dst + kScaleOff, a.k_scale + row0, kChunk * 4, bar, policy);
+    bulk_g2s_hint(dst + kScaleOff + kChunk * 4, a.v_scale + row0, kChunk * 4, bar, policy);
+  }
+
+  __device__ static void load_q(Regs& r, const DecodeArgs& a, int32_t b, int32_t h, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    const uint2* qrow = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                       (static_cast<int64_t>(b) * a.Hq + h * G + g) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (g < G) {
+        const uint2 w = __ldg(qrow + 4 * ks + t);   // dims 16ks + 4t .. +3
+        r.qa[ks][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+        r.qa[ks][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+      } else {
+        r.qa[ks][0] = r.qa[ks][1] = 0u;
+      }
+    }
+  }
+
+  __device__ static void reset(Regs& r) {
+    r.m = -INFINITY;
+    r.l = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) r.o[n][0] = r.o[n][1] = r.o[n][2] = r.o[n][3] = 0.f;
+  }
+
+  __device__ static void chunk(Regs& r, const unsigned char* stage, int vlo, int vhi, float scale_log2, int lane) {
+    const uint32_t kb = smem_addr(stage);
+    const uint32_t vb = kb + KBOX;
+    const float* scl = reinterpret_cast<const float*>(stage + kScaleOff);
+    const int t = lane & 3;
+    const int mi = lane >> 3, mr = lane & 7;
+    float s[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      const int tok = 4 * (mr >> 1) + (mr & 1) + 2 * nt;
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t w[4];
+        ldsm_x4(kb + tok * 128 + (((4 * p + mi) ^ (tok & 7)) << 4), w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_f16_16816(s[nt], r.qa[4 * p + j][0], 0u, r.qa[4 * p + j][1], 0u, e4m3x2_to_f16x2(w[j]),
+                        e4m3x2_to_f16x2(w[j] >> 16));
+      }
+    }
+    const float4 ksc = *reinterpret_cast<const float4*>(scl + 4 * t);
+    const float4 vsc = *reinterpret_cast<const float4*>(scl + kChunk + 4 * t);
+    const bool ok0 = 4 * t >= vlo && 4 * t < vhi, ok1 = 4 * t + 1 >= vlo && 4 * t + 1 < vhi;
+    const bool ok2 = 4 * t + 2 >= vlo && 4 * t + 2 < vhi, ok3 = 4 * t + 3 >= vlo && 4 * t + 3 < vhi;
+    float x[4];
+    x[0] = ok0 ? s[0][0] * ksc.x * scale_log2 : -INFINITY;
+    x[1] = ok1 ? s[0][1] * ksc.y * scale_log2 : -INFINITY;
+    x[2] = ok2 ? s[1][0] * ksc.z * scale_log2 : -INFINITY;
+    x[3] = ok3 ? s[1][1] * ksc.w * scale_log2 : -INFINITY;
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const bool raise = mx > r.m + kRescaleLog2;
+    if (__any_sync(0xffffffffu, raise)) {
+      const float mnew = raise ? mx : r.m;
+      const float alpha = exp2f(r.m - mnew);
+      r.m = mnew;
+      r.l *= alpha;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        r.o[n][0] *= alpha;
+        r.o[n][1] *= alpha;
+        r.o[n][2] *= alpha;
+        r.o[n][3] *= alpha;
+      }
+    }
+    float pr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pr[e] = exp2f(x[e] - r.m);
+    r.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    // a masked token's scale may be garbage (even NaN): select 0 rather than multiply
+    const float p0 = ok0 ? pr[0] * vsc.x * kPScale : 0.f, p1 = ok1 ? pr[1] * vsc.y * kPScale : 0.f;
+    const float p2 = ok2 ? pr[2] * vsc.z * kPScale : 0.f, p3 = ok3 ? pr[3] * vsc.w * kPScale : 0.f;
+    const uint32_t hi0 = pack_f16x2(p0, p1), hi1 = pack_f16x2(p2, p3);
+    const uint32_t lo0 = pack_f16x2(p0 - f16_lo(hi0), p1 - f16_hi(hi0));
+    const uint32_t lo1 = pack_f16x2(p2 - f16_lo(hi1), p3 - f16_hi(hi1));
+    uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
+    if (vlo > 0 || vhi < kChunk) {  // zero V entries of tokens outside the range (they may hold NaN)
+      mask01 = (ok0 ? 0x0000ffffu : 0u) | (ok1 ? 0xffff0000u : 0u);
+      mask23 = (ok2 ? 0x0000ffffu : 0u) | (ok3 ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int q4 = 0; q4 < NT / 4; ++q4) {
+      uint32_t v[4];
+      ldsm_x4(vb + (8 * (4 * q4 + mi) + mr) * kChunk, v[0], v[1], v[2], v[3]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        mma_f16_16816(r.o[4 * q4 + j], hi0, lo0, hi1, lo1, e4m3x2_to_f16x2(v[j]) & mask01,
+                      e4m3x2_to_f16x2(v[j] >> 16) & mask23);
+    }
+  }
+
+  __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float lt = r.l;
+    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+    if (g >= G) return;
+    const float inv = 1.f / (lt * kPScale);
 #pragma unroll
     for (int n = 0; n < NT; ++n)
       *reinterpret_cast<float2*>(dst + g * D + 8 * n + 2 * t) =

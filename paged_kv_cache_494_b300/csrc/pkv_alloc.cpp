@@ -113,7 +113,8 @@ pkv_status pkv_pool_create(const pkv_pool_desc* d, pkv_pool** out) {
   if (!d || !out) return PKV_ERR_INVALID;
   *out = nullptr;
   if (d->num_layers < 1 || d->num_kv_heads < 1 || d->head_dim < 1 || d->block_size < 1 || d->num_blocks < 1 ||
-      d->max_seqs < 1 || d->max_blocks_per_seq < 1 || (d->dtype != PKV_F32 && d->dtype != PKV_BF16))
+      d->max_seqs < 1 || d->max_blocks_per_seq < 1 ||
+      (d->dtype != PKV_F32 && d->dtype != PKV_BF16 && d->dtype != PKV_FP8))
     return PKV_ERR_INVALID;
   pkv_pool* p = new (std::nothrow) pkv_pool();
   if (!p) return PKV_ERR_INVALID;
@@ -149,7 +150,14 @@ void pkv_pool_destroy(pkv_pool* p) { delete p; }
 
 int64_t pkv_bytes_per_token(const pkv_pool* p) {
   if (!p) return 0;
-  return 2LL * p->desc.num_layers * p->desc.num_kv_heads * p->desc.head_dim * pkv::elem_bytes(p->desc.dtype);
+  const int64_t codes = 2LL * p->desc.num_layers * p->desc.num_kv_heads * p->desc.head_dim * pkv::elem_bytes(p->desc.dtype);
+  const int64_t scales = p->desc.dtype == PKV_FP8 ? 2LL * p->desc.num_layers * p->desc.num_kv_heads * 4 : 0;
+  return codes + scales;
+}
+
+int64_t pkv_layer_scale_bytes(const pkv_pool* p) {
+  if (!p || p->desc.dtype != PKV_FP8) return 0;
+  return static_cast<int64_t>(p->desc.num_blocks) * p->desc.num_kv_heads * p->desc.block_size * 4;
 }
 
 int64_t pkv_layer_cache_bytes(const pkv_pool* p) {

@@ -77,40 +77,42 @@ int env_int(const char* name, int fallback) {
 using DecodeKernel = void (*)(DecodeArgs, pkv_dev::TmaMaps);
 using ReduceKernel = void (*)(DecodeArgs);
 
+enum MapKind { MAPS_NONE = 0, MAPS_BF16 = 1, MAPS_FP8 = 2 };
+
 struct KernelPair {
   DecodeKernel decode = nullptr;
   ReduceKernel reduce = nullptr;
   int stage_bytes = 0;
-  bool tensor_maps = false;   // bf16 tensor-core path (K/V staged by 2-D tensor TMA)
+  int maps = MAPS_NONE;   // which tensor maps the staging needs (1-D bulk copies when none)
 };
 
 template <class Math, int D, int G>
-KernelPair pair_for(bool tmaps) {
+KernelPair pair_for(int maps) {
   KernelPair k;
   k.decode = pkv_dev::paged_decode_kernel<Math, D, G>;
   k.reduce = pkv_dev::decode_reduce_kernel<D, G>;
   k.stage_bytes = Math::kStageBytes;
-  k.tensor_maps = tmaps;
+  k.maps = maps;
   return k;
 }
 
 template <int D, int G>
 KernelPair pick_bf16(bool simt) {
-  if (simt) return pair_for<pkv_dev::SimtMath<__nv_bfloat16, D, G>, D, G>(false);
-  return pair_for<pkv_dev::MmaMath<D, G>, D, G>(true);
+  if (simt) return pair_for<pkv_dev::SimtMath<__nv_bfloat16, D, G>, D, G>(MAPS_NONE);
+  return pair_for<pkv_dev::MmaMath<D, G>, D, G>(MAPS_BF16);
 }
 
 template <int D>
 KernelPair pick_g(int dtype, int g, bool simt) {
   if (dtype == PKV_F32) {
     switch (g) {
-      case 1: return pair_for<pkv_dev::SimtMath<float, D, 1>, D, 1>(false);
-      case 2: return pair_for<pkv_dev::SimtMath<float, D, 2>, D, 2>(false);
-      case 3: return pair_for<pkv_dev::SimtMath<float, D, 3>, D, 3>(false);
-      case 4: return pair_for<pkv_dev::SimtMath<float, D, 4>, D, 4>(false);
-      case 5: return pair_for<pkv_dev::SimtMath<float, D, 5>, D, 5>(false);
-      case 6: return pair_for<pkv_dev::SimtMath<float, D, 6>, D, 6>(false);
-      case 8: return pair_for<pkv_dev::SimtMath<float, D, 8>, D, 8>(false);
+      case 1: return pair_for<pkv_dev::SimtMath<float, D, 1>, D, 1>(MAPS_NONE);
+      case 2: return pair_for<pkv_dev::SimtMath<float, D, 2>, D, 2>(MAPS_NONE);
+      case 3: return pair_for<pkv_dev::SimtMath<float, D, 3>, D, 3>(MAPS_NONE);
+      case 4: return pair_for<pkv_dev::SimtMath<float, D, 4>, D, 4>(MAPS_NONE);
+      case 5: return pair_for<pkv_dev::SimtMath<float, D, 5>, D, 5>(MAPS_NONE);
+      case 6: return pair_for<pkv_dev::SimtMath<float, D, 6>, D, 6>(MAPS_NONE);
+      case 8: return pair_for<pkv_dev::SimtMath<float, D, 8>, D, 8>(MAPS_NONE);
       default: return KernelPair{};
     }
   }
@@ -133,7 +135,22 @@ bool force_simt() {
   return s && std::strcmp(s, "simt") == 0;
 }
 
+KernelPair pick_fp8(int g) {
+  switch (g) {
+    case 1: return pair_for<pkv_dev::Fp8Math<1>, 128, 1>(MAPS_FP8);
+    case 2: return pair_for<pkv_dev::Fp8Math<2>, 128, 2>(MAPS_FP8);
+    case 3: return pair_for<pkv_dev::Fp8Math<3>, 128, 3>(MAPS_FP8);
+    case 4: return pair_for<pkv_dev::Fp8Math<4>, 128, 4>(MAPS_FP8);
+    case 5: return pair_for<pkv_dev::Fp8Math<5>, 128, 5>(MAPS_FP8);
+    case 6: return pair_for<pkv_dev::Fp8Math<6>, 128, 6>(MAPS_FP8);
+    case 7: return pair_for<pkv_dev::Fp8Math<7>, 128, 7>(MAPS_FP8);
+    case 8: return pair_for<pkv_dev::Fp8Math<8>, 128, 8>(MAPS_FP8);
+    default: return KernelPair{};
+  }
+}
+
 KernelPair pick_kernels(int dtype, int D, int g) {
+  if (dtype == PKV_FP8) return D == 128 ? pick_fp8(g) : KernelPair{};
   if (dtype != PKV_F32 && dtype != PKV_BF16) return KernelPair{};
   const bool simt = force_simt();
   if (dtype == PKV_F32 && g == 7) return KernelPair{};
@@ -168,6 +185,30 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const pkv_pool_desc& d) 
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp8 pools: K codes as a 2-D uint8 [NB*Hkv*B rows][D] array (boxes of 16 rows x 128 bytes, 128-byte
+// swizzle); V codes as a 2-D uint8 [NB*Hkv*D rows][B] array (dim-major pages; boxes of 128 rows x
+// 16 bytes, no swizzle).
+bool encode_fp8_maps(pkv_dev::TmaMaps* maps, const void* k_cache, const void* v_cache, const pkv_pool_desc& d) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || d.head_dim != 128) return false;
+  cuuint32_t estr[2] = {1, 1};
+  cuuint64_t kdims[2] = {static_cast<cuuint64_t>(d.head_dim),
+                         static_cast<cuuint64_t>(d.num_blocks) * d.num_kv_heads * d.block_size};
+  cuuint64_t kstr[1] = {static_cast<cuuint64_t>(d.head_dim)};
+  cuuint32_t kbox[2] = {128, static_cast<cuuint32_t>(pkv_dev::kChunk)};
+  if (fn(&maps->k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(k_cache), kdims, kstr, kbox, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cuuint64_t vdims[2] = {static_cast<cuuint64_t>(d.block_size),
+                         static_cast<cuuint64_t>(d.num_blocks) * d.num_kv_heads * d.head_dim};
+  cuuint64_t vstr[1] = {static_cast<cuuint64_t>(d.block_size)};
+  cuuint32_t vbox[2] = {static_cast<cuuint32_t>(pkv_dev::kChunk), static_cast<cuuint32_t>(d.head_dim)};
+  return fn(&maps->v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), vdims, vstr, vbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -235,6 +276,12 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   return PKV_OK;
 }
 
+pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                         const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads, float scale,
+                         int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -247,6 +294,7 @@ pkv_status pkv_reshape_and_cache(const pkv_pool* p, const void* k, const void* v
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(slots) & 7u))
     return PKV_ERR_INVALID;
   const pkv_pool_desc& d = p->desc;
+  if (d.dtype == PKV_FP8) return PKV_ERR_INVALID;   // fp8 pools quantise: pkv_reshape_and_cache_fp8
   const int row_bytes = d.head_dim * pkv::elem_bytes(d.dtype);
   if (row_bytes % 16 != 0) return PKV_ERR_INVALID;
   const int ppr = row_bytes / 16;
@@ -267,6 +315,7 @@ pkv_status pkv_copy_blocks(const pkv_pool* p, void* const* k_caches, void* const
   if (!p || n_pairs < 0) return PKV_ERR_INVALID;
   if (n_pairs == 0) return PKV_OK;
   const pkv_pool_desc& d = p->desc;
+  if (d.dtype == PKV_FP8) return PKV_ERR_INVALID;   // fp8 blocks carry scales: pkv_copy_blocks_fp8
   if (!k_caches || !v_caches || !pairs || d.num_layers > pkv_dev::kMaxLayers) return PKV_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(pairs) & 7u) return PKV_ERR_INVALID;
   pkv_dev::LayerCaches lc;
@@ -371,6 +420,91 @@ pkv_status pkv_paged_decode_window(const pkv_pool* p, float* out, const void* q,
                                    const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                                    int32_t n_seqs, int32_t num_q_heads, float scale, int32_t window,
                                    int32_t partition_tokens, void* workspace, size_t workspace_bytes, void* stream) {
+  if (p && p->desc.dtype == PKV_FP8) return PKV_ERR_INVALID;   // pkv_paged_decode_fp8
+  return decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs,
+                       num_q_heads, scale, window, partition_tokens, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_decode_fp8(const pkv_pool* p, float* out, const void* q, const void* k_cache,
+                                const void* v_cache, const float* k_scale, const float* v_scale,
+                                const int32_t* block_tables, const int32_t* context_lens, int32_t n_seqs,
+                                int32_t num_q_heads, float scale, int32_t window, int32_t partition_tokens,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  if (!p || p->desc.dtype != PKV_FP8) return PKV_ERR_INVALID;
+  if (n_seqs > 0 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale))) return PKV_ERR_INVALID;
+  return decode_launch(p, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, n_seqs,
+                       num_q_heads, scale, window, partition_tokens, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_reshape_and_cache_fp8(const pkv_pool* p, const void* k, const void* v, const int64_t* slots,
+                                     int32_t n_tokens, void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                     void* stream) {
+  if (!p || n_tokens < 0 || p->desc.dtype != PKV_FP8) return PKV_ERR_INVALID;
+  if (n_tokens == 0) return PKV_OK;
+  const pkv_pool_desc& d = p->desc;
+  if (d.head_dim != 64 && d.head_dim != 128) return PKV_ERR_INVALID;
+  if (!k || !v || !slots || !k_cache || !v_cache || !k_scale || !v_scale) return PKV_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
+      !aligned16(v_scale) || (reinterpret_cast<uintptr_t>(slots) & 7u))
+    return PKV_ERR_INVALID;
+  const int64_t rows = static_cast<int64_t>(n_tokens) * d.num_kv_heads;
+  const int warps_per_cta = 8;
+  const int64_t want = (rows + warps_per_cta - 1) / warps_per_cta;
+  const int grid = static_cast<int>(want < 65535 * 4 ? want : 65535 * 4);
+  auto kern = d.head_dim == 128 ? pkv_dev::reshape_and_cache_fp8_kernel<128> : pkv_dev::reshape_and_cache_fp8_kernel<64>;
+  const cudaError_t e = launch(kern, dim3(grid), dim3(32 * warps_per_cta), 0, static_cast<cudaStream_t>(stream),
+                               static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slots,
+                               n_tokens, d.num_kv_heads, d.block_size,
+                               static_cast<int64_t>(d.num_blocks) * d.block_size, static_cast<uint8_t*>(k_cache),
+                               static_cast<uint8_t*>(v_cache), k_scale, v_scale);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks_fp8(const pkv_pool* p, void* const* k_caches, void* const* v_caches,
+                               void* const* k_scales, void* const* v_scales, const int32_t* pairs, int32_t n_pairs,
+                               void* stream) {
+  if (!p || n_pairs < 0 || p->desc.dtype != PKV_FP8) return PKV_ERR_INVALID;
+  if (n_pairs == 0) return PKV_OK;
+  const pkv_pool_desc& d = p->desc;
+  if (!k_caches || !v_caches || !k_scales || !v_scales || !pairs || d.num_layers > pkv_dev::kMaxLayers)
+    return PKV_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(pairs) & 7u) return PKV_ERR_INVALID;
+  pkv_dev::LayerCaches codes, scales;
+  std::memset(&codes, 0, sizeof codes);
+  std::memset(&scales, 0, sizeof scales);
+  for (int l = 0; l < d.num_layers; ++l) {
+    if (!k_caches[l] || !v_caches[l] || !k_scales[l] || !v_scales[l] || !aligned16(k_caches[l]) ||
+        !aligned16(v_caches[l]) || !aligned16(k_scales[l]) || !aligned16(v_scales[l]))
+      return PKV_ERR_INVALID;
+    codes.k[l] = static_cast<uint4*>(k_caches[l]);
+    codes.v[l] = static_cast<uint4*>(v_caches[l]);
+    scales.k[l] = static_cast<uint4*>(k_scales[l]);
+    scales.v[l] = static_cast<uint4*>(v_scales[l]);
+  }
+  const int64_t code_bytes = static_cast<int64_t>(d.num_kv_heads) * d.block_size * d.head_dim;
+  const int64_t scale_bytes = static_cast<int64_t>(d.num_kv_heads) * d.block_size * 4;
+  if (code_bytes % 16 != 0 || scale_bytes % 16 != 0) return PKV_ERR_INVALID;
+  const int64_t grid = static_cast<int64_t>(n_pairs) * d.num_layers;
+  if (grid > 0x7fffffff) return PKV_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch(pkv_dev::copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, codes, pairs,
+             d.num_layers, code_bytes / 16, d.num_blocks) != cudaSuccess ||
+      launch(pkv_dev::copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, scales, pairs,
+             d.num_layers, scale_bytes / 16, d.num_blocks) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                         const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads, float scale,
+                         int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                         void* stream) {
   if (!p || window < 0) return PKV_ERR_INVALID;
   if (n_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID;
@@ -409,11 +543,18 @@ pkv_status pkv_paged_decode_window(const pkv_pool* p, float* out, const void* q,
   a.scale_log2 = scale * 1.4426950408889634f;
   pkv_dev::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
-  if (pl.k.tensor_maps) {
-    const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size;
+  if (pl.k.maps != MAPS_NONE) {
+    const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size *
+                         (pl.k.maps == MAPS_FP8 ? d.head_dim / d.block_size + 1 : 1);
     if (rows > 0x7fffffffLL) return PKV_ERR_INVALID;   // tensor coordinates are 32-bit
-    if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d)) return PKV_ERR_CUDA;
+    if (pl.k.maps == MAPS_BF16) {
+      if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d)) return PKV_ERR_CUDA;
+    } else if (!encode_fp8_maps(&maps, k_cache, v_cache, d)) {
+      return PKV_ERR_CUDA;
+    }
   }
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t reduce_ctas = (pl.n_units + pkv_dev::kReduceWarps - 1) / pkv_dev::kReduceWarps;
   if (reduce_ctas > 0x7fffffff) return PKV_ERR_INVALID;
@@ -426,6 +567,10 @@ pkv_status pkv_paged_decode_window(const pkv_pool* p, float* out, const void* q,
     return PKV_ERR_CUDA;
   return PKV_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 pkv_status pkv_last_error(const pkv_pool*) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;

@@ -61,5 +61,5 @@ struct pkv_pool {
 };
 
 namespace pkv {
-inline int elem_bytes(int32_t dtype) { return dtype == PKV_F32 ? 4 : 2; }
+inline int elem_bytes(int32_t dtype) { return dtype == PKV_F32 ? 4 : (dtype == PKV_FP8 ? 1 : 2); }
 }  // namespace pkv

@@ -15,6 +15,7 @@ import synth
 from oracle import alloc_model as am
 from oracle import cache_ops as ocache
 from oracle import native
+from oracle import fp8 as _ofp8  # noqa: F401
 
 TOL = {"f32": 1e-5, "bf16": 2e-3}
 
@@ -214,3 +215,120 @@ def case_from_workload(name: str, seed: Optional[int] = None, host_cache: bool =
         kw["prefix_trace"] = synth.prefix_trace(w, seed)
         kw["max_blocks"] = -(-int(lens.max()) // w.block_size) + 1
     return Case(**kw)
+
+
+class Fp8Case:
+    """An fp8 pool built on both sides: the library quantises bf16 K/V on the device; the oracle
+    quantises the same decoded values on the host (oracle/fp8.py). Unwritten memory is poisoned
+    (NaN codes and scales) on both sides."""
+
+    def __init__(self, *, lengths, Hq, Hkv, B=16, D=128, seed=0, num_blocks=None, prefix_trace=None):
+        from oracle import fp8 as ofp8
+        self.ofp8 = ofp8
+        self.Hq, self.Hkv, self.D, self.B, self.seed = Hq, Hkv, D, B, seed
+        lengths = [int(x) for x in lengths]
+        pages = sum(-(-L // B) for L in lengths)
+        self.NB = num_blocks or max(pages + 4 * len(lengths) + 8, 16)
+        self.MB = max(max(-(-L // B) for L in lengths), 1) + 4
+        self.scale = 1.0 / math.sqrt(D)
+        fl = synth.free_list(self.NB, seed)
+        n_ids = len(lengths) + 1
+        self.pool = pkv.Pool(1, Hkv, D, B, self.NB, n_ids, self.MB, pkv.FP8, initial_free_list=fl)
+        self.model = am.PoolModel(self.NB, B, n_ids, self.MB, initial_free_list=fl)
+        ks, vs, ss = self.pool.fp8_shapes()
+        self.k8 = torch.full(ks, 0x7F, dtype=torch.uint8, device="cuda")
+        self.v8 = torch.full(vs, 0x7F, dtype=torch.uint8, device="cuda")
+        self.ksc = torch.full(ss, float("nan"), device="cuda")
+        self.vsc = torch.full(ss, float("nan"), device="cuda")
+        self.hk8 = np.full(ks, 0x7F, np.uint8)
+        self.hv8 = np.full(vs, 0x7F, np.uint8)
+        self.hks = np.full(ss, np.nan, np.float32)
+        self.hvs = np.full(ss, np.nan, np.float32)
+        self._stream = 0
+        if prefix_trace is None:
+            self.seqs = [self._append(-1, L) for L in lengths]
+        else:
+            children, root = {}, None
+            for op in prefix_trace:
+                if op[0] == "new":
+                    root = self._append(-1, op[1])
+                elif op[0] == "fork":
+                    c = self.pool.fork(root)
+                    assert self.model.fork(root) == (am.OK, c)
+                    children[len(children)] = c
+                elif op[0] == "free":
+                    self.pool.free(root)
+                    self.model.free_seq(root)
+                else:
+                    self._append(children[op[1]], op[2])
+            self.seqs = [children[i] for i in range(len(children))]
+        self.n = len(self.seqs)
+        self.q_stored = synth.encode(synth.normal_f32((self.n, Hq, D), seed, 7), "bf16")
+        self.q = to_device(self.q_stored, "bf16")
+        self.refresh_tables()
+
+    def refresh_tables(self):
+        tables, lens = self.pool.block_table(self.seqs)
+        mtab, mlens = self.model.block_table(self.seqs)
+        assert tables.tolist() == mtab and lens.tolist() == mlens
+        self.tables = torch.from_numpy(tables).cuda()
+        self.lens = torch.from_numpy(lens).cuda()
+        self.oracle_tables = np.asarray(mtab, dtype=np.int32)
+        self.oracle_lens = np.asarray(mlens, dtype=np.int32)
+
+    def _append(self, seq, n_tokens, magnitude=None):
+        sid, slots, pairs = self.pool.alloc(seq, n_tokens)
+        st, msid, mslots, mpairs = self.model.alloc(seq, n_tokens)
+        assert st == am.OK and msid == sid and slots.tolist() == mslots and pairs == mpairs
+        self._stream += 1
+        kv = synth.normal_f32((2, n_tokens, self.Hkv, self.D), self.seed, 2000 + self._stream)
+        # a spread of row magnitudes, and an all-zero row, exercise the per-row scales
+        kv *= np.exp(synth.normal_f32((2, n_tokens, self.Hkv, 1), self.seed, 3000 + self._stream))
+        if n_tokens > 3:
+            kv[:, 3] = 0.0
+        k, v = synth.encode(kv[0], "bf16"), synth.encode(kv[1], "bf16")
+        if pairs:
+            d_pairs = torch.tensor(np.asarray(pairs, dtype=np.int32).reshape(-1, 2), device="cuda")
+            self.pool.copy_blocks_fp8([self.k8], [self.v8], [self.ksc], [self.vsc], d_pairs)
+            for src, dst in mpairs:
+                for arr in (self.hk8, self.hv8, self.hks, self.hvs):
+                    arr[dst] = arr[src]
+        if n_tokens:
+            self.pool.reshape_and_cache_fp8(to_device(k, "bf16"), to_device(v, "bf16"),
+                                            torch.from_numpy(slots.copy()).cuda(), self.k8, self.v8, self.ksc,
+                                            self.vsc)
+            self.ofp8.reshape_and_cache_fp8(self.hk8, self.hks, self.hv8, self.hvs, synth.bf16_bits_to_f32(k),
+                                            synth.bf16_bits_to_f32(v), mslots)
+        return sid
+
+    def decode_step_append(self):
+        slots, pairs = self.pool.append(self.seqs)
+        st, mslots, mpairs = self.model.append(self.seqs)
+        assert st == am.OK and slots.tolist() == mslots
+        self._stream += 1
+        kv = synth.normal_f32((2, self.n, self.Hkv, self.D), self.seed, 5000 + self._stream)
+        k, v = synth.encode(kv[0], "bf16"), synth.encode(kv[1], "bf16")
+        if len(pairs):
+            self.pool.copy_blocks_fp8([self.k8], [self.v8], [self.ksc], [self.vsc],
+                                      torch.from_numpy(np.ascontiguousarray(pairs, dtype=np.int32)).cuda())
+            for src, dst in mpairs:
+                for arr in (self.hk8, self.hv8, self.hks, self.hvs):
+                    arr[dst] = arr[src]
+        self.pool.reshape_and_cache_fp8(to_device(k, "bf16"), to_device(v, "bf16"), torch.from_numpy(slots).cuda(),
+                                        self.k8, self.v8, self.ksc, self.vsc)
+        self.ofp8.reshape_and_cache_fp8(self.hk8, self.hks, self.hv8, self.hvs, synth.bf16_bits_to_f32(k),
+                                        synth.bf16_bits_to_f32(v), mslots)
+        self.refresh_tables()
+
+    def gpu_decode(self, partition_tokens=0, window=0):
+        out = torch.full((self.n, self.Hq, self.D), float("nan"), device="cuda")
+        nbytes = self.pool.decode_workspace_bytes(self.n, self.Hq, partition_tokens)
+        ws = torch.empty(max(nbytes, 16) // 4 + 4, device="cuda")
+        self.pool.paged_decode_fp8(out, self.q, self.k8, self.v8, self.ksc, self.vsc, self.tables, self.lens,
+                                   self.scale, window=window, partition_tokens=partition_tokens, workspace=ws)
+        torch.cuda.synchronize()
+        return out
+
+    def oracle_decode(self, window=0):
+        K, V = self.ofp8.dequantize_pool(self.hk8, self.hks, self.hv8, self.hvs)
+        return native.decode(self.q_stored, K, V, self.oracle_tables, self.oracle_lens, self.scale, window=window)

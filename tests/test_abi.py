@@ -54,6 +54,14 @@ def test_sizes_follow_the_budget_formula():
     assert 2 * p.num_layers * p.layer_cache_bytes == 100 * 16 * p.bytes_per_token
 
 
+def test_fp8_sizes():
+    p = pkv.Pool(32, 8, 128, 16, 100, 4, 8, pkv.FP8)
+    assert p.layer_cache_bytes == 100 * 8 * 16 * 128
+    assert p.layer_scale_bytes == 100 * 8 * 16 * 4
+    assert p.bytes_per_token == 2 * 32 * 8 * (128 + 4)          # codes + one scale per token and head
+    assert pkv.Pool(1, 2, 64, 16, 4, 1, 1, pkv.BF16).layer_scale_bytes == 0
+
+
 def test_invalid_descriptors_rejected():
     import pytest
     with pytest.raises(pkv.PagedKVError):
