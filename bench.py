@@ -594,31 +594,44 @@ def bench_prefill(args):
 
 
 def profile_decode(args):
-    """Small case for ncu: one layer of the workload (about 0.8 GB of KV, above L2), decode x5."""
+    """Small case for ncu: one layer of the serving workload (about 0.8 GB of bf16 KV, 0.4 GB of fp8,
+    above L2), decode x5. --workload serve256_fp8 profiles the fp8 pool."""
     import torch
     import paged_kv_cache_494_b300 as pkv
+    fp8 = args.workload == "serve256_fp8"
     w = synth.workload(WORKLOAD)
     lens = synth.lengths(w, args.seed)
     NB = synth.pool_blocks(w, lens)
     MB = -(-int(lens.max()) // w.block_size) + 1
-    pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs, MB, pkv.BF16,
+    pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs, MB, pkv.FP8 if fp8 else pkv.BF16,
                     initial_free_list=synth.free_list(NB, args.seed))
     seqs = [pool.alloc(-1, int(t))[0] for t in lens]
     tables, l = pool.block_table(seqs)
     g = torch.Generator(device="cuda").manual_seed(args.seed)
     shape = (NB, w.num_kv_heads, w.block_size, w.head_dim)
-    kc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
-    vc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
+    if fp8:
+        ks_, vs_, ss_ = pool.fp8_shapes()
+        kc = torch.randint(0, 0x7E, ks_, device="cuda", dtype=torch.uint8, generator=g)
+        vc = torch.randint(0, 0x7E, vs_, device="cuda", dtype=torch.uint8, generator=g)
+        ksc = torch.rand(ss_, device="cuda", generator=g) * 0.01
+        vsc = torch.rand(ss_, device="cuda", generator=g) * 0.01
+    else:
+        kc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
+        vc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
     q = torch.randn(w.n_seqs, w.num_q_heads, w.head_dim, device="cuda", dtype=torch.bfloat16, generator=g)
     out = torch.empty(w.n_seqs, w.num_q_heads, w.head_dim, device="cuda")
     ws = torch.empty(pool.decode_workspace_bytes(w.n_seqs, w.num_q_heads, 0) // 4 + 4, device="cuda")
     t_tab, t_len = torch.from_numpy(tables).cuda(), torch.from_numpy(l).cuda()
     for _ in range(5):
-        pool.paged_decode(out, q, kc, vc, t_tab, t_len, w.scale, 0, ws)
+        if fp8:
+            pool.paged_decode_fp8(out, q, kc, vc, ksc, vsc, t_tab, t_len, w.scale, 0, 0, ws)
+        else:
+            pool.paged_decode(out, q, kc, vc, t_tab, t_len, w.scale, 0, ws)
     torch.cuda.synchronize()
     assert pkv.last_error() == pkv.OK
-    kv = int(l.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
-    print(json.dumps({"profile_decode": WORKLOAD, "layers": 1, "kv_bytes_per_launch": kv, "NB": NB}))
+    per = (w.head_dim + 4) * 2 if fp8 else w.head_dim * 2 * 2
+    kv = int(l.sum()) * w.num_kv_heads * per
+    print(json.dumps({"profile_decode": args.workload, "layers": 1, "kv_bytes_per_launch": kv, "NB": NB}))
 
 
 def main(argv=None):
