@@ -67,7 +67,8 @@ typedef enum {
 
 /* Storage type of a pool. PKV_FP8: K and V as FP8 E4M3 codes with one float32 scale per (token,
  * KV head) for K and one for V; q stays bf16. FP8 layouts: k_cache [NB][Hkv][B][D] codes (token-major
- * like the others), v_cache [NB][Hkv][D][B] codes (dim-major within a page), k_scale / v_scale
+ * like the others), v_cache [NB][Hkv][D][B] codes (dim-major within a page; each 16-token group of
+ * a dim row in the token order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15), k_scale / v_scale
  * [NB][Hkv][B] float32. Quantising the cache is one of the cache strategies ("¿Cuánta memoria reservar
  * para la caché KV?", "Adaptar el presupuesto a la estrategia de caché"); it changes the numerics, so
  * fp8 pools use the *_fp8 entry points and their own contract. */

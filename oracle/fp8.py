@@ -66,13 +66,24 @@ def dequantize(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return decode_e4m3(codes) * np.asarray(scale, dtype=np.float64)[..., None]
 
 
+# Byte position, within a 16-token group of a dim-major V page, of token j (a layout convention of
+# the library's fp8 pools): the group is stored in the token order 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15.
+V_GROUP_ORDER = [0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15]
+V_POSITION = [V_GROUP_ORDER.index(j) for j in range(16)]
+
+
+def v_byte_offset(off: int) -> int:
+    """Byte position of in-block token offset ``off`` in a dim-major V page row."""
+    return (off - off % 16) + V_POSITION[off % 16]
+
+
 def reshape_and_cache_fp8(k8: np.ndarray, ks: np.ndarray, v8t: np.ndarray, vs: np.ndarray, k: np.ndarray,
                           v: np.ndarray, slots) -> None:
     """Quantise new K/V rows and scatter them into an fp8 pool, in place.
 
     Layout (the library's): k8 [NB][Hkv][B][D] codes, v8t [NB][Hkv][D][B] codes (V stored dim-major
-    within a page), ks / vs [NB][Hkv][B] float32 scales. k, v: [n_tokens][Hkv][D] float32 values
-    (decoded bf16 inputs). A negative slot skips its token.
+    within a page, 16-token groups in the order V_GROUP_ORDER), ks / vs [NB][Hkv][B] float32 scales.
+    k, v: [n_tokens][Hkv][D] float32 values (decoded bf16 inputs). A negative slot skips its token.
     """
     B = k8.shape[2]
     kc, ksc = quantize_rows(k)
@@ -84,12 +95,14 @@ def reshape_and_cache_fp8(k8: np.ndarray, ks: np.ndarray, v8t: np.ndarray, vs: n
         blk, off = s // B, s % B
         k8[blk, :, off, :] = kc[i]
         ks[blk, :, off] = ksc[i]
-        v8t[blk, :, :, off] = vc[i]
+        v8t[blk, :, :, v_byte_offset(off)] = vc[i]
         vs[blk, :, off] = vsc[i]
 
 
 def dequantize_pool(k8: np.ndarray, ks: np.ndarray, v8t: np.ndarray, vs: np.ndarray):
     """float64 K and V caches in the standard [NB][Hkv][B][D] layout from an fp8 pool."""
     K = decode_e4m3(k8) * ks.astype(np.float64)[..., None]
-    V = decode_e4m3(np.swapaxes(v8t, 2, 3)) * vs.astype(np.float64)[..., None]
+    B = v8t.shape[3]
+    tok_order = np.array([v_byte_offset(off) for off in range(B)])
+    V = decode_e4m3(np.swapaxes(v8t[..., tok_order], 2, 3)) * vs.astype(np.float64)[..., None]
     return K, V

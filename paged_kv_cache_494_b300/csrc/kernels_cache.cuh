@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(LayerCaches caches, co
 // Per row: amax = max |x|, scale = amax / 448 (IEEE division; 1 when amax == 0), codes =
 // e4m3(x / scale) rounded to nearest even with saturation. K rows are stored token-major
 // (k8[blk][h][off][:]), V rows dim-major within the page (v8t[blk][h][d][off]); the scales go to
-// ks / vs [blk][h][off]. Quantising the cache is one of the pages' cache strategies ("¿Cuánta memoria
+// ks / vs [blk][h][off] (V codes of a 16-token group in the order 0,1,8,9,2,3,10,11,... so that
+// the decode's fragments line up). Quantising the cache is one of the pages' cache strategies ("¿Cuánta memoria
 // reservar para la caché KV?", "Adaptar el presupuesto a la estrategia de caché").
 template <int D>
 __device__ __forceinline__ float quantize_lane(const __nv_bfloat16* row, int lane, uint32_t* codes_out) {
@@ -136,8 +137,12 @@ __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
     } else {
       *reinterpret_cast<uint16_t*>(kdst) = static_cast<uint16_t>(kw);
     }
+    // V: dim-major page; within each 16-token group the byte order of tokens is
+    // (0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15)
+    const int64_t j = off & 15;
+    const int64_t pos = (off - j) + (j < 8 ? 4 * (j >> 1) + (j & 1) : 4 * ((j - 8) >> 1) + 2 + (j & 1));
 #pragma unroll
-    for (int e = 0; e < E; ++e) v8t[(page * D + E * lane + e) * B + off] = static_cast<uint8_t>(vw >> (8 * e));
+    for (int e = 0; e < E; ++e) v8t[(page * D + E * lane + e) * B + pos] = static_cast<uint8_t>(vw >> (8 * e));
     if (lane == 0) {
       ks[page * B + off] = kscale;
       vs[page * B + off] = vscale;

@@ -20,9 +20,12 @@
 //    free of bank conflicts, and computes q.K and p.V with mma.sync (m16n8k16, fp32 accumulate);
 //    the fp32 path uses 1-D bulk copies and CUDA-core dot products with warp shuffles.
 //  * A segment is the part of a unit one warp processes. A segment that is a whole unit writes the
-//    output directly; otherwise it writes (m, l, o/l) to the workspace and the reduce kernel merges
-//    the segments of the unit: M = max m_k, w_k = l_k 2^(m_k - M), o = sum w_k o_k / sum w_k.
-//    m is kept in log2 units (scores pre-multiplied by scale * log2 e), which changes no result.
+//    output directly; otherwise it writes (m, l, o/l) to the workspace and arrives on the unit's
+//    counter; the warp that arrives last merges the unit's segments: M = max m_k,
+//    w_k = l_k 2^(m_k - M), o = sum w_k o_k / sum w_k. m is kept in log2 units (scores
+//    pre-multiplied by scale * log2 e), which changes no result. Counters carry a tag unique to the
+//    call in their high 48 bits, so they never need clearing: a count left by an earlier call (or
+//    never written) carries another tag and restarts at 1.
 //  * The split depends only on the context lengths, never on physical block ids, so results are
 //    bitwise invariant under any placement of the blocks.
 #pragma once
@@ -50,7 +53,7 @@ struct DecodeArgs {
   const int32_t* context_lens;   // [n_seqs]
   float* ws_ml;                  // [n_slots][G][2]  (m in log2 units, l)
   float* ws_o;                   // [n_slots][G][D]  (o already divided by l)
-  int32_t* ws_desc;              // balanced mode: [n_units][2]
+  unsigned long long* ws_count;  // [n_units] arrival counters: (call tag << 16) | segments arrived
   int32_t n_seqs, Hq, Hkv, B, NB, MB;
   int32_t part_chunks;           // 0: balanced split; > 0: chunks per partition
   int32_t max_parts;             // fixed mode: partition slots per unit
@@ -60,7 +63,109 @@ struct DecodeArgs {
   float scale_log2;              // scale * log2(e)
   const float* k_scale;          // fp8 pools: [NB][Hkv][B] per-(token, head) scales (else unused)
   const float* v_scale;
+  unsigned long long tag;        // 48-bit tag of this call for ws_count
 };
+
+// Arrival of one segment of a split unit. Returns true for the warp that completes the unit.
+// Lock-free: the CAS only fails when another segment arrived in between.
+__device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long tag, int64_t n_parts) {
+  unsigned long long old = atomicAdd(ctr, 0ull), assumed, next;
+  do {
+    assumed = old;
+    next = ((assumed >> 16) == tag) ? assumed + 1 : ((tag << 16) | 1ull);
+    old = atomicCAS(ctr, assumed, next);
+  } while (old != assumed);
+  return static_cast<int64_t>(next & 0xffffull) == n_parts;
+}
+
+// Log-sum-exp merge of one unit's n_parts segments by one warp. Segment k's slot is
+// 2 * (wf + k) + (k == 0 ? first_kind : 0) in balanced mode (part_chunks == 0), else
+// u * max_parts + k. kWide loads all of a segment's values before combining them (more registers,
+// one memory latency per segment); the narrow form works through them one float4 at a time.
+template <int D, int G, bool kWide>
+__device__ __noinline__ void merge_unit(const DecodeArgs& a, int32_t b, int32_t h, int64_t n_parts, int64_t wf,
+                                        int first_kind, int lane) {
+  const int64_t u = static_cast<int64_t>(b) * a.Hkv + h;
+  auto slot_of = [&](int64_t k) -> int64_t {
+    return a.part_chunks != 0 ? u * a.max_parts + k : 2 * (wf + k) + (k == 0 ? first_kind : 0);
+  };
+  constexpr int V4 = G * D / 4;  // float4 values per unit
+  constexpr int R = kWide ? (V4 + 31) / 32 : 1;
+  if constexpr (!kWide) {
+#pragma unroll 1
+    for (int idx = lane; idx < V4; idx += 32) {
+      const int j = idx / (D / 4);
+      float M = -INFINITY, wsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+      for (int64_t k = 0; k < n_parts; ++k) {
+        const int64_t sl = slot_of(k);
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (sl * G + j) * 2));
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (sl * G + j) * D) + (idx - j * (D / 4)));
+        const float Mn = fmaxf(M, ml.x);
+        const float c = exp2f(M - Mn);
+        const float wk = ml.y * exp2f(ml.x - Mn);
+        acc.x = fmaf(wk, o.x, acc.x * c);
+        acc.y = fmaf(wk, o.y, acc.y * c);
+        acc.z = fmaf(wk, o.z, acc.z * c);
+        acc.w = fmaf(wk, o.w, acc.w * c);
+        wsum = fmaf(wsum, c, wk);
+        M = Mn;
+      }
+      const float inv = 1.f / wsum;
+      reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[idx - j * (D / 4)] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    return;
+  }
+  float M[R], wsum[R];
+  float4 acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    M[r] = -INFINITY;
+    wsum[r] = 0.f;
+    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll 2
+  for (int64_t k = 0; k < n_parts; ++k) {
+    const int64_t s = slot_of(k);
+    float2 ml[R];
+    float4 o[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {  // all of this segment's loads first (L2: written by other warps)
+      const int idx = lane + 32 * r;
+      if (idx < V4) {
+        const int j = idx / (D / 4);
+        ml[r] = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2));
+        o[r] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D) + (idx - j * (D / 4)));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (lane + 32 * r < V4) {
+        const float Mn = fmaxf(M[r], ml[r].x);
+        const float c = exp2f(M[r] - Mn);  // rescales what was accumulated so far (0 at the start)
+        const float wk = ml[r].y * exp2f(ml[r].x - Mn);
+        acc[r].x = fmaf(wk, o[r].x, acc[r].x * c);
+        acc[r].y = fmaf(wk, o[r].y, acc[r].y * c);
+        acc[r].z = fmaf(wk, o[r].z, acc[r].z * c);
+        acc[r].w = fmaf(wk, o[r].w, acc[r].w * c);
+        wsum[r] = fmaf(wsum[r], c, wk);
+        M[r] = Mn;
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int idx = lane + 32 * r;
+    if (idx < V4) {
+      const int j = idx / (D / 4);
+      const float inv = 1.f / wsum[r];
+      reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[idx - j * (D / 4)] =
+          make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
+    }
+  }
+}
 
 __device__ __forceinline__ int32_t clamped_len(const DecodeArgs& a, int32_t b) {
   int32_t len = __ldg(a.context_lens + b);
@@ -223,6 +328,7 @@ struct SimtMath {
   static constexpr int PIECES = EPL / PER16;
   static constexpr int CB = kChunk * D * es;  // bytes of one K (or V) chunk
   static constexpr int kStageBytes = 2 * CB;
+  static constexpr int kMinCtasPerSm = 1;     // register-heavy: let the compiler use up to 255
   static_assert(LPT * EPL == D && TPP * LPT == 32 && PASSES * TPP == kChunk, "lane layout");
   static_assert(PIECES * PER16 == EPL, "pieces");
 
@@ -382,6 +488,7 @@ struct MmaMath {
   static constexpr int BOX = kChunk * 128;   // one box: 16 rows x 128 bytes
   static constexpr int CB = KB * BOX;        // K (or V) chunk bytes
   static constexpr int kStageBytes = 2 * CB;
+  static constexpr int kMinCtasPerSm = 3;    // 12 warps per SM: the register budget is 168 per thread
   static constexpr int KS = D / 16;          // k-steps of q.K
   static constexpr int NT = D / 8;           // n-tiles of p.V
   static constexpr float kRescaleLog2 = 8.f;
@@ -436,16 +543,18 @@ struct MmaMath {
     float s[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      float se[4] = {0.f, 0.f, 0.f, 0.f}, so[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-steps: half-length chains
       const int tok = 8 * nt + mr;
 #pragma unroll
       for (int p = 0; p < KS / 2; ++p) {
         const int db = 4 * p + mi;                      // 16-byte block of 8 dims
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kb + (db >> 3) * BOX + swz(tok, db & 7), b0, b1, b2, b3);
-        mma_bf16_16816(s[nt], r.qa[2 * p][0], 0u, r.qa[2 * p][1], 0u, b0, b1);
-        mma_bf16_16816(s[nt], r.qa[2 * p + 1][0], 0u, r.qa[2 * p + 1][1], 0u, b2, b3);
+        mma_bf16_16816(se, r.qa[2 * p][0], 0u, r.qa[2 * p][1], 0u, b0, b1);
+        mma_bf16_16816(so, r.qa[2 * p + 1][0], 0u, r.qa[2 * p + 1][1], 0u, b2, b3);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = se[e] + so[e];
     }
     // ---- online softmax for head g over tokens {2t, 2t+1, 8+2t, 9+2t}
     float x[4];
@@ -522,10 +631,10 @@ struct MmaMath {
 // dim-major in fp8 pools)][16 K scales][16 V scales], padded to 5120 bytes.
 // q.K: the contraction over d is order-free, so within each 16-dim k-step lane t takes dims
 // 4t..4t+3 for both operands: ldmatrix on the fp8 rows hands each lane 4 consecutive codes, which
-// cvt turns into the two f16 pairs of its B fragment; q is loaded with the same dim order. The
-// n-tiles hold tokens {0,1,4,5,8,9,12,13} and {2,3,6,7,10,11,14,15}, so lane t's scores are tokens
-// 4t..4t+3 and its P fragment matches the V fragment ldmatrix reads from the dim-major V box
-// (tokens 4t..4t+3 of one dim). Per-token scales: S *= k_scale; P' = p * v_scale * 1024 is split
+// cvt turns into the two f16 pairs of its B fragment; q is loaded with the same dim order. p.V: the
+// fp8 V page stores each 16-token group in the order (0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15), so
+// the 4 codes ldmatrix hands lane t from a dim row are tokens (2t, 2t+1, 8+2t, 9+2t): exactly the
+// tokens of lane t's scores and of its P fragment. Per-token scales: S *= k_scale; P' = p * v_scale * 1024 is split
 // into f16 hi + lo (rows 0..7 / 8..15); the running max is raised when a chunk exceeds it by 2^2,
 // so p <= 4 and P' stays inside the f16 normal range for |V| < ~7000.
 // ------------------------------------------------------------------------------------------------
@@ -538,6 +647,7 @@ struct Fp8Math {
   static constexpr int kScaleOff = KBOX + VBOX;
   static constexpr int kTxBytes = KBOX + VBOX + 2 * kChunk * 4;
   static constexpr int kStageBytes = 5120;
+  static constexpr int kMinCtasPerSm = 3;
   static constexpr int KS = D / 16;
   static constexpr int NT = D / 8;
   static constexpr float kRescaleLog2 = 2.f;
@@ -592,22 +702,29 @@ struct Fp8Math {
     float s[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-      const int tok = 4 * (mr >> 1) + (mr & 1) + 2 * nt;
+      float se[4] = {0.f, 0.f, 0.f, 0.f}, so[4] = {0.f, 0.f, 0.f, 0.f};
+      const int tok = 8 * nt + mr;
 #pragma unroll
       for (int p = 0; p < 2; ++p) {
         uint32_t w[4];
         ldsm_x4(kb + tok * 128 + (((4 * p + mi) ^ (tok & 7)) << 4), w[0], w[1], w[2], w[3]);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          mma_f16_16816(s[nt], r.qa[4 * p + j][0], 0u, r.qa[4 * p + j][1], 0u, e4m3x2_to_f16x2(w[j]),
+          mma_f16_16816((j & 1) ? so : se, r.qa[4 * p + j][0], 0u, r.qa[4 * p + j][1], 0u, e4m3x2_to_f16x2(w[j]),
                         e4m3x2_to_f16x2(w[j] >> 16));
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = se[e] + so[e];
     }
-    const float4 ksc = *reinterpret_cast<const float4*>(scl + 4 * t);
-    const float4 vsc = *reinterpret_cast<const float4*>(scl + kChunk + 4 * t);
-    const bool ok0 = 4 * t >= vlo && 4 * t < vhi, ok1 = 4 * t + 1 >= vlo && 4 * t + 1 < vhi;
-    const bool ok2 = 4 * t + 2 >= vlo && 4 * t + 2 < vhi, ok3 = 4 * t + 3 >= vlo && 4 * t + 3 < vhi;
+    // this lane's tokens: 2t, 2t+1 (n-tile 0) and 8+2t, 9+2t (n-tile 1)
+    const float2 ksa = *reinterpret_cast<const float2*>(scl + 2 * t);
+    const float2 ksb = *reinterpret_cast<const float2*>(scl + 8 + 2 * t);
+    const float2 vsa = *reinterpret_cast<const float2*>(scl + kChunk + 2 * t);
+    const float2 vsb = *reinterpret_cast<const float2*>(scl + kChunk + 8 + 2 * t);
+    const float4 ksc = make_float4(ksa.x, ksa.y, ksb.x, ksb.y);
+    const float4 vsc = make_float4(vsa.x, vsa.y, vsb.x, vsb.y);
+    const bool ok0 = 2 * t >= vlo && 2 * t < vhi, ok1 = 2 * t + 1 >= vlo && 2 * t + 1 < vhi;
+    const bool ok2 = 8 + 2 * t >= vlo && 8 + 2 * t < vhi, ok3 = 9 + 2 * t >= vlo && 9 + 2 * t < vhi;
     float x[4];
     x[0] = ok0 ? s[0][0] * ksc.x * scale_log2 : -INFINITY;
     x[1] = ok1 ? s[0][1] * ksc.y * scale_log2 : -INFINITY;
@@ -679,7 +796,7 @@ struct Fp8Math {
 // per-warp TMA ring, segment bookkeeping and output / partial writes. Math is a policy.
 // ------------------------------------------------------------------------------------------------
 template <class Math, int D, int G>
-__global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant__ DecodeArgs a,
+__global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(const __grid_constant__ DecodeArgs a,
                                                            const __grid_constant__ TmaMaps maps) {
   constexpr int SB = Math::kStageBytes;
   const int lane = threadIdx.x & 31;
@@ -710,17 +827,15 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
   const int w = blockIdx.x * NW + warp;
   const int64_t NP = static_cast<int64_t>(pref[n]) * Hkv;
 
-  // Empty sequences: zero rows (and mark their units complete for the reduce).
+  // Empty sequences: zero rows.
   for (int32_t b = w; b < n; b += W) {
     if (pref[b + 1] != pref[b]) continue;
     float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(b) * a.Hq * D);
     for (int i = lane; i < a.Hq * D / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (PC == 0)
-      for (int32_t h = lane; h < Hkv; h += 32) a.ws_desc[2 * (static_cast<int64_t>(b) * Hkv + h)] = -1;
   }
 
   // Balanced mode splits the chunks over Weff = min(W, NP) warps so that every range between a
-  // unit's first and last warp is non-empty (the reduce relies on it).
+  // unit's first and last warp is non-empty (the merge relies on it).
   const int64_t Weff = NP < W ? NP : W;
   int64_t lo, hi;
   if (PC == 0) {
@@ -774,23 +889,12 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
   int32_t seg_c0 = cc.c;
   int seg_idx = 0;
 
-  auto write_desc = [&](int64_t x) {  // balanced mode, at the first chunk of a unit
-    if (PC != 0 || lane != 0) return;
-    const int64_t e_u = x + cc.nch;
-    const int64_t u = static_cast<int64_t>(cc.b) * Hkv + cc.h;
-    if (e_u <= hi) {
-      a.ws_desc[2 * u] = -1;
-    } else {
-      const int64_t w_last = (e_u * Weff - 1) / NP;
-      a.ws_desc[2 * u] = (w << 1) | (seg_idx == 0 ? 0 : 1);
-      a.ws_desc[2 * u + 1] = static_cast<int32_t>(w_last);
-    }
-  };
-
   int32_t len_b = clamped_len(a, cc.b);
   Math::load_q(r, a, cc.b, cc.h, lane);
   Math::reset(r);
-  if (cc.c == 0) write_desc(lo);
+  bool pend = false;  // this warp completed a split unit with its last segment: merge it at the end
+  int32_t pend_b = 0, pend_h = 0, pend_kind = 0;
+  int64_t pend_parts = 0, pend_wf = 0;
 
   bool aborted = false;
   int64_t i = 0;
@@ -821,6 +925,36 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
         const int64_t slot = (PC == 0) ? (2 * static_cast<int64_t>(w) + (seg_idx == 0 ? 0 : 1))
                                        : (u * a.max_parts + cc.c / PC);
         Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
+        // Segments of this unit: balanced mode, warps warp_of(s_u) .. warp_of(e_u - 1) where
+        // warp_of(p) = floor(((p + 1) * Weff - 1) / NP); fixed mode, its partitions.
+        int64_t n_parts, wf = 0;
+        int first_kind = 0;
+        if (PC == 0) {
+          const int64_t s_u = static_cast<int64_t>(pref[cc.b]) * Hkv + static_cast<int64_t>(cc.h) * cc.nch;
+          const int64_t e_u = s_u + cc.nch;
+          wf = ((s_u + 1) * Weff - 1) / NP;
+          n_parts = (e_u * Weff - 1) / NP - wf + 1;
+          first_kind = (s_u == NP * wf / Weff) ? 0 : 1;
+        } else {
+          n_parts = (cc.nch + PC - 1) / PC;
+        }
+        __threadfence();  // this segment's partial is visible before the arrival
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = arrive_last(a.ws_count + u, a.tag, n_parts) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence();
+          if (range_end) {  // the usual case: merge after the loop, when its registers are free
+            pend = true;
+            pend_b = cc.b;
+            pend_h = cc.h;
+            pend_parts = n_parts;
+            pend_wf = wf;
+            pend_kind = first_kind;
+          } else {
+            merge_unit<D, G, false>(a, cc.b, cc.h, n_parts, wf, first_kind, lane);
+          }
+        }
       }
       ++seg_idx;
     }
@@ -831,7 +965,6 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
         if (unit_end) {
           if (cc.b != prev_b) len_b = clamped_len(a, cc.b);
           Math::load_q(r, a, cc.b, cc.h, lane);
-          if (cc.c == 0) write_desc(lo + i + 1);
         }
         Math::reset(r);
         seg_c0 = cc.c;
@@ -844,98 +977,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const __grid_constant
       mbar_wait_bounded(smem_addr(bars + static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1));
   }
   pdl_launch_dependents();
-}
-
-// ------------------------------------------------------------------------------------------------
-// Log-sum-exp merge of the segments of split units: one warp per unit (b, h), 8 warps per CTA.
-// Online form over the segments (running max M, weight sum, accumulator), so every segment's
-// loads are independent of the previous segment's arithmetic and can be in flight together.
-// ------------------------------------------------------------------------------------------------
-constexpr int kReduceWarps = 8;
-
-template <int D, int G>
-__global__ void __launch_bounds__(32 * kReduceWarps) decode_reduce_kernel(const __grid_constant__ DecodeArgs a) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const int64_t u = static_cast<int64_t>(blockIdx.x) * kReduceWarps + (threadIdx.x >> 5);
-  if (u >= static_cast<int64_t>(a.n_seqs) * a.Hkv) return;
-  const int32_t b = static_cast<int32_t>(u / a.Hkv);
-  const int32_t h = static_cast<int32_t>(u - static_cast<int64_t>(b) * a.Hkv);
-  int64_t first_slot, n_parts;
-  int32_t first_kind = 0;
-  if (a.part_chunks == 0) {
-    const int32_t d0 = a.ws_desc[2 * u];
-    if (d0 < 0) return;
-    first_slot = d0 >> 1;          // warp id of the first segment
-    first_kind = d0 & 1;
-    const int32_t w_last = a.ws_desc[2 * u + 1];
-    if (w_last < first_slot || w_last >= a.total_warps) {   // never written by a finished decode
-      if (lane == 0) record_error(ERRBIT_BOUNDS);
-      return;
-    }
-    n_parts = w_last - first_slot + 1;
-  } else {
-    const int32_t len = clamped_len(a, b);
-    const int32_t c0 = (a.window > 0 && len > a.window) ? (len - a.window) / kChunk : 0;
-    const int32_t nch = (len + kChunk - 1) / kChunk - c0;
-    n_parts = (nch + a.part_chunks - 1) / a.part_chunks;
-    if (n_parts <= 1) return;
-    if (n_parts > a.max_parts) {
-      if (lane == 0) record_error(ERRBIT_BOUNDS);
-      return;
-    }
-    first_slot = u * a.max_parts;
-  }
-  constexpr int V4 = G * D / 4;          // float4 values per unit
-  constexpr int R = (V4 + 31) / 32;       // per lane
-  float M[R], wsum[R];
-  float4 acc[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    M[r] = -INFINITY;
-    wsum[r] = 0.f;
-    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-#pragma unroll 2
-  for (int64_t k = 0; k < n_parts; ++k) {
-    const int64_t s = (a.part_chunks != 0) ? first_slot + k : 2 * (first_slot + k) + (k == 0 ? first_kind : 0);
-    float2 ml[R];
-    float4 o[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {      // all of this segment's loads first
-      const int idx = lane + 32 * r;
-      if (idx < V4) {
-        const int j = idx / (D / 4);
-        ml[r] = *reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2);
-        o[r] = reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D)[idx - j * (D / 4)];
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (lane + 32 * r < V4) {
-        const float Mn = fmaxf(M[r], ml[r].x);
-        const float c = exp2f(M[r] - Mn);  // rescales what was accumulated so far (0 at the start)
-        const float wk = ml[r].y * exp2f(ml[r].x - Mn);
-        acc[r].x = fmaf(wk, o[r].x, acc[r].x * c);
-        acc[r].y = fmaf(wk, o[r].y, acc[r].y * c);
-        acc[r].z = fmaf(wk, o[r].z, acc[r].z * c);
-        acc[r].w = fmaf(wk, o[r].w, acc[r].w * c);
-        wsum[r] = fmaf(wsum[r], c, wk);
-        M[r] = Mn;
-      }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int idx = lane + 32 * r;
-    if (idx < V4) {
-      const int j = idx / (D / 4);
-      const float inv = 1.f / wsum[r];
-      reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[idx - j * (D / 4)] =
-          make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
-    }
-  }
+  if (pend) merge_unit<D, G, true>(a, pend_b, pend_h, pend_parts, pend_wf, pend_kind, lane);
 }
 
 }  // namespace pkv_dev

@@ -7,7 +7,9 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <chrono>
 #include <cstdint>
+#include <random>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -75,13 +77,11 @@ int env_int(const char* name, int fallback) {
 // decode planning
 // ---------------------------------------------------------------------------------------------
 using DecodeKernel = void (*)(DecodeArgs, pkv_dev::TmaMaps);
-using ReduceKernel = void (*)(DecodeArgs);
 
 enum MapKind { MAPS_NONE = 0, MAPS_BF16 = 1, MAPS_FP8 = 2 };
 
 struct KernelPair {
   DecodeKernel decode = nullptr;
-  ReduceKernel reduce = nullptr;
   int stage_bytes = 0;
   int maps = MAPS_NONE;   // which tensor maps the staging needs (1-D bulk copies when none)
 };
@@ -90,7 +90,6 @@ template <class Math, int D, int G>
 KernelPair pair_for(int maps) {
   KernelPair k;
   k.decode = pkv_dev::paged_decode_kernel<Math, D, G>;
-  k.reduce = pkv_dev::decode_reduce_kernel<D, G>;
   k.stage_bytes = Math::kStageBytes;
   k.maps = maps;
   return k;
@@ -238,6 +237,18 @@ struct DecodePlan {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Tag of a decode call for the workspace's arrival counters: 48 bits, odd (so never the zero of fresh
+// memory) and distinct for 2^47 consecutive calls of the process (2 * counter + 1, the counter
+// started at a random point), so counts left by earlier calls are never taken for this call's.
+unsigned long long next_call_tag() {
+  static std::atomic<unsigned long long> counter{[] {
+    std::random_device rd;
+    return (static_cast<unsigned long long>(rd()) << 20) ^
+           static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count());
+  }()};
+  return ((counter.fetch_add(1, std::memory_order_relaxed) << 1) | 1ull) & 0xffffffffffffull;
+}
+
 pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t partition_tokens, DecodePlan* out) {
   const pkv_pool_desc& d = p->desc;
   if (n_seqs < 0 || Hq <= 0 || Hq % d.num_kv_heads != 0) return PKV_ERR_INVALID;
@@ -268,8 +279,9 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   } else {
     pl.n_slots = 2 * static_cast<int64_t>(pl.warps);
   }
-  const size_t desc_bytes = partition_tokens > 0 ? 0 : static_cast<size_t>(pl.n_units) * 2 * sizeof(int32_t);
-  pl.off_ml = round_up(desc_bytes, 256);
+  if (pl.max_parts > 0xffff || pl.warps > 0xffff) return PKV_ERR_INVALID;   // 16-bit arrival counts
+  const size_t count_bytes = static_cast<size_t>(pl.n_units) * sizeof(unsigned long long);
+  pl.off_ml = round_up(count_bytes, 256);
   pl.off_o = pl.off_ml + round_up(static_cast<size_t>(pl.n_slots) * g * 2 * sizeof(float), 256);
   pl.ws_bytes = pl.off_o + static_cast<size_t>(pl.n_slots) * g * d.head_dim * sizeof(float);
   *out = pl;
@@ -526,7 +538,7 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   a.block_tables = block_tables;
   a.context_lens = context_lens;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  a.ws_desc = reinterpret_cast<int32_t*>(ws);
+  a.ws_count = reinterpret_cast<unsigned long long*>(ws);
   a.ws_ml = reinterpret_cast<float*>(ws + pl.off_ml);
   a.ws_o = reinterpret_cast<float*>(ws + pl.off_o);
   a.n_seqs = n_seqs;
@@ -555,14 +567,9 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   }
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.tag = next_call_tag();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t reduce_ctas = (pl.n_units + pkv_dev::kReduceWarps - 1) / pkv_dev::kReduceWarps;
-  if (reduce_ctas > 0x7fffffff) return PKV_ERR_INVALID;
   if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||
-      cudaGetLastError() != cudaSuccess)
-    return PKV_ERR_CUDA;
-  if (launch(pl.k.reduce, dim3(static_cast<unsigned>(reduce_ctas)), dim3(32 * pkv_dev::kReduceWarps), 0, s, a) !=
-          cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;

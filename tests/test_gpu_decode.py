@@ -88,6 +88,33 @@ def test_permutation_invariance_bitwise(path):
         assert torch.equal(c1.gpu_decode(pt), c2.gpu_decode(pt))
 
 
+def test_workspace_reused_by_consecutive_calls_bitwise(path):
+    """One workspace serves many calls in a row, alternating split modes and problem sizes.
+
+    Each call's arrival counters must ignore the counts its predecessors left behind, so every call
+    returns exactly what it returns on a fresh NaN-filled workspace.
+    """
+    c = case_from_workload("gqa5_bf16", host_cache=False)
+    nbytes = max(c.pool.decode_workspace_bytes(c.n, c.Hq, pt) for pt in (0, 512, 64))
+
+    def run(pt, n, ws):
+        out = torch.full((n, c.Hq, c.D), float("nan"), dtype=torch.float32, device="cuda")
+        c.pool.paged_decode(out, c.q[:n], c.k_cache, c.v_cache, c.tables[:n], c.lens[:n], c.scale,
+                            partition_tokens=pt, workspace=ws)
+        torch.cuda.synchronize()
+        return out
+
+    def nan_ws():
+        return torch.full((nbytes // 4 + 4,), float("nan"), dtype=torch.float32, device="cuda")
+
+    sizes = (c.n, c.n // 2)                         # a shorter batch leaves stale counters behind
+    fresh = {(pt, n): run(pt, n, nan_ws()) for pt in (0, 512, 64) for n in sizes}
+    ws = nan_ws()
+    for it in range(12):
+        pt, n = (0, 512, 64)[it % 3], sizes[it % 2]
+        assert torch.equal(run(pt, n, ws), fresh[(pt, n)]), (it, pt, n)
+
+
 def test_shared_prefix_equals_duplicated_bitwise():
     """Same logical data: prefix pages shared through forks vs private copies written separately."""
     B, H, D = 16, 8, 128

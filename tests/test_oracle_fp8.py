@@ -77,7 +77,7 @@ def test_quantising_scatter_and_dequantised_attention():
     for i, sl in enumerate(slots):
         assert np.array_equal(K[sl // B, :, sl % B], fp8.dequantize(kq[i], ksc[i]))
         assert np.array_equal(V[sl // B, :, sl % B], fp8.dequantize(vq[i], vsc[i]))
-        assert np.array_equal(v8t[sl // B, :, :, sl % B], vq[i])
+        assert np.array_equal(v8t[sl // B, :, :, fp8.v_byte_offset(sl % B)], vq[i])
     tables = np.array([[5, 2]], np.int32)
     q = rng.standard_normal((1, 4, D)).astype(np.float32)
     a = att.paged_decode(q, K, V, tables, [20], 1 / math.sqrt(D))
@@ -88,3 +88,11 @@ def test_quantising_scatter_and_dequantised_attention():
     for j in range(4):
         np.testing.assert_allclose(a[0, j], att.dense_attention(q[0, j].astype(np.float64), Kc[j // 2], Vc[j // 2],
                                                                 1 / math.sqrt(D)), rtol=0, atol=1e-14)
+
+
+def test_v_group_order_is_a_permutation():
+    assert sorted(fp8.V_GROUP_ORDER) == list(range(16))
+    assert [fp8.v_byte_offset(j) for j in range(32)][16:] == [16 + p for p in fp8.V_POSITION]
+    # lane t of a dim row reads bytes 4t..4t+3: tokens (2t, 2t+1, 8+2t, 9+2t)
+    for t in range(4):
+        assert fp8.V_GROUP_ORDER[4 * t:4 * t + 4] == [2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t]
