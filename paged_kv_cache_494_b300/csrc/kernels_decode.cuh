@@ -68,8 +68,20 @@ struct DecodeArgs {
 
 // Arrival of one segment of a split unit. Returns true for the warp that completes the unit.
 // Lock-free: the CAS only fails when another segment arrived in between.
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long tag, int64_t n_parts) {
-  unsigned long long old = atomicAdd(ctr, 0ull), assumed, next;
+  unsigned long long old = ld_relaxed_gpu(ctr), assumed, next;
   do {
     assumed = old;
     next = ((assumed >> 16) == tag) ? assumed + 1 : ((tag << 16) | 1ull);
@@ -329,6 +341,7 @@ struct SimtMath {
   static constexpr int CB = kChunk * D * es;  // bytes of one K (or V) chunk
   static constexpr int kStageBytes = 2 * CB;
   static constexpr int kMinCtasPerSm = 1;     // register-heavy: let the compiler use up to 255
+  static constexpr int kQElem = es;
   static_assert(LPT * EPL == D && TPP * LPT == 32 && PASSES * TPP == kChunk, "lane layout");
   static_assert(PIECES * PER16 == EPL, "pieces");
 
@@ -468,14 +481,19 @@ struct SimtMath {
 };
 
 // ------------------------------------------------------------------------------------------------
-// Tensor-core math for bf16 caches, G <= 8 query heads per KV head.
+// Tensor-core math for bf16 caches, G <= 8 query heads per KV head, in transposed form: the 16-row
+// side of m16n8k16 is filled by 16 tokens (scores) or 16 dims (output) and the heads sit on the
+// 8-wide side, so no mma row is padding.
 //
-// S = Q K^T per 16-token chunk: A = Q (rows = the G heads, zero-padded to 16), B = K chunk read
-// with ldmatrix from the swizzled boxes, fp32 accumulate: 2 n-tiles x D/16 k-steps of m16n8k16.
-// O += P V: A rows 0..7 hold P rounded to bf16 (hi) and rows 8..15 hold the rounding remainder
-// (lo = bf16(P - hi)), so one mma accumulates both and hi + lo carries P to ~2^-17 relative;
-// B = V chunk read with ldmatrix.trans. Lane (g = lane/4, t = lane%4) owns head g, tokens
-// {2t, 2t+1, 8+2t, 9+2t} of each chunk and output dims {8n + 2t, 8n + 2t + 1}.
+// S^T = K q^T per 16-token chunk: A = the K chunk (rows = tokens) read with ldmatrix from the
+// swizzled boxes, B = q^T (column n = a head), fp32 accumulate: D/16 mma. O^T += V^T P^T: A = V^T
+// read with ldmatrix.trans (16 dims per m-tile), B = P^T, which movmatrix.trans makes from the
+// score fragment: D/16 m-tiles. P is carried as bf16 hi + lo (lo = bf16(P - hi)), ~2^-17 relative.
+// With G <= 4 the 8 columns hold every head twice: the lanes of columns 0..3 pass hi, those of
+// columns 4..7 (same scores, same maxima) pass lo, so one mma per m-tile accumulates both and the
+// halves are added at the end; with G > 4 each m-tile takes a second mma for lo.
+// Lane (g = lane/4, t = lane%4) owns columns {2t, 2t+1}: the scores of tokens {g, g+8} and the
+// output dims {16i + g, 16i + g + 8}; its running max and sum belong to those two columns.
 // The running max is raised only when a chunk's max exceeds it by more than kRescaleLog2 (the
 // exponentials then stay below 2^kRescaleLog2), which skips most rescales of O without changing
 // the result: numerator and denominator always use the same max.
@@ -489,15 +507,22 @@ struct MmaMath {
   static constexpr int CB = KB * BOX;        // K (or V) chunk bytes
   static constexpr int kStageBytes = 2 * CB;
   static constexpr int kMinCtasPerSm = 3;    // 12 warps per SM: the register budget is 168 per thread
-  static constexpr int KS = D / 16;          // k-steps of q.K
-  static constexpr int NT = D / 8;           // n-tiles of p.V
+  static constexpr int KS = D / 16;          // k-steps of q.K and m-tiles of p.V
+  static constexpr bool kPaired = G <= 4;    // columns 4..7 repeat heads 0..3 and carry lo
   static constexpr float kRescaleLog2 = 8.f;
+  static constexpr int kQElem = 2;
 
   struct Regs {
-    uint32_t qa[KS][2];  // A fragment registers 0 and 2 (rows 8..15 are zero)
-    float o[NT][4];      // [0..1]: hi part (row g), [2..3]: lo part (row g + 8)
-    float m, l;          // running max (log2 units) and this lane's share of the sum, head g
+    uint32_t qb[KS][2];  // B fragment of q^T: head of column g, dims 16ks + {2t, 2t+1} and {+8, +9}
+    float o[KS][4];      // O^T: dims 16i + g ([0], [1]) and 16i + g + 8 ([2], [3]); columns 2t, 2t+1
+    float m[2], l[2];    // running max (log2 units) and this lane's share of the sum, per column
   };
+
+  // Head carried by column n, or -1 for a padding column.
+  __device__ static __forceinline__ int head_of(int n) {
+    const int hd = kPaired ? (n & 3) : n;
+    return hd < G ? hd : -1;
+  }
 
   __device__ static void issue(const DecodeArgs&, const TmaMaps& maps, uint32_t dst, uint32_t bar, int64_t row0,
                                uint64_t policy) {
@@ -512,20 +537,21 @@ struct MmaMath {
 
   __device__ static void load_q(Regs& r, const DecodeArgs& a, int32_t b, int32_t h, int lane) {
     const int g = lane >> 2, t = lane & 3;
-    const uint32_t* qrow =
-        reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) + (static_cast<int64_t>(b) * a.Hq + h * G + g) * D);
+    const int hd = head_of(g);
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                             (static_cast<int64_t>(b) * a.Hq + h * G + max(hd, 0)) * D);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      r.qa[ks][0] = g < G ? __ldg(qrow + 8 * ks + t) : 0u;
-      r.qa[ks][1] = g < G ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+      r.qb[ks][0] = hd >= 0 ? __ldg(qrow + 8 * ks + t) : 0u;
+      r.qb[ks][1] = hd >= 0 ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
     }
   }
 
   __device__ static void reset(Regs& r) {
-    r.m = -INFINITY;
-    r.l = 0.f;
+    r.m[0] = r.m[1] = -INFINITY;
+    r.l[0] = r.l[1] = 0.f;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) r.o[n][0] = r.o[n][1] = r.o[n][2] = r.o[n][3] = 0.f;
+    for (int i = 0; i < KS; ++i) r.o[i][0] = r.o[i][1] = r.o[i][2] = r.o[i][3] = 0.f;
   }
 
   // Byte offset of 16-byte block `cb` (0..7) of row `row` inside a 128B-swizzled box.
@@ -537,106 +563,151 @@ struct MmaMath {
   __device__ static void chunk(Regs& r, const unsigned char* kbase, int vlo, int vhi, float scale_log2, int lane) {
     const uint32_t kb = smem_addr(kbase);
     const uint32_t vb = kb + CB;
-    const int t = lane & 3;
+    const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix index and row of this lane's address
-    // ---- S = Q K^T
-    float s[2][4];
+    // ---- S^T = K q^T (two accumulators: half-length dependency chains)
+    float se[4] = {0.f, 0.f, 0.f, 0.f}, so[4] = {0.f, 0.f, 0.f, 0.f};
+    const int ktok = mr + 8 * (mi & 1);       // matrices 0, 2: tokens 0..7; 1, 3: tokens 8..15
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float se[4] = {0.f, 0.f, 0.f, 0.f}, so[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-steps: half-length chains
-      const int tok = 8 * nt + mr;
-#pragma unroll
-      for (int p = 0; p < KS / 2; ++p) {
-        const int db = 4 * p + mi;                      // 16-byte block of 8 dims
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + (db >> 3) * BOX + swz(tok, db & 7), b0, b1, b2, b3);
-        mma_bf16_16816(se, r.qa[2 * p][0], 0u, r.qa[2 * p][1], 0u, b0, b1);
-        mma_bf16_16816(so, r.qa[2 * p + 1][0], 0u, r.qa[2 * p + 1][1], 0u, b2, b3);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = se[e] + so[e];
+    for (int ks = 0; ks < KS; ++ks) {
+      const int db = 2 * ks + (mi >> 1);      // matrices 0, 1: dims 16ks..+7; 2, 3: dims 16ks+8..+15
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kb + (db >> 3) * BOX + swz(ktok, db & 7), a0, a1, a2, a3);
+      if (ks & 1)
+        mma_bf16_16816(so, a0, a1, a2, a3, r.qb[ks][0], r.qb[ks][1]);
+      else
+        mma_bf16_16816(se, a0, a1, a2, a3, r.qb[ks][0], r.qb[ks][1]);
     }
-    // ---- online softmax for head g over tokens {2t, 2t+1, 8+2t, 9+2t}
+    // ---- online softmax per column over tokens {g, g+8} of every lane
+    const bool okg = g >= vlo && g < vhi, okg8 = g + 8 >= vlo && g + 8 < vhi;
     float x[4];
-    const bool ok0 = 2 * t >= vlo && 2 * t < vhi, ok1 = 2 * t + 1 >= vlo && 2 * t + 1 < vhi;
-    const bool ok2 = 8 + 2 * t >= vlo && 8 + 2 * t < vhi, ok3 = 9 + 2 * t >= vlo && 9 + 2 * t < vhi;
-    x[0] = ok0 ? s[0][0] * scale_log2 : -INFINITY;
-    x[1] = ok1 ? s[0][1] * scale_log2 : -INFINITY;
-    x[2] = ok2 ? s[1][0] * scale_log2 : -INFINITY;
-    x[3] = ok3 ? s[1][1] * scale_log2 : -INFINITY;
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const bool raise = mx > r.m + kRescaleLog2;
-    if (__any_sync(0xffffffffu, raise)) {
-      const float mnew = raise ? mx : r.m;
-      const float alpha = exp2f(r.m - mnew);  // 0 on the first chunk (m = -inf), 1 if unchanged
-      r.m = mnew;
-      r.l *= alpha;
+    x[0] = okg ? (se[0] + so[0]) * scale_log2 : -INFINITY;
+    x[1] = okg ? (se[1] + so[1]) * scale_log2 : -INFINITY;
+    x[2] = okg8 ? (se[2] + so[2]) * scale_log2 : -INFINITY;
+    x[3] = okg8 ? (se[3] + so[3]) * scale_log2 : -INFINITY;
+    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        r.o[n][0] *= alpha;
-        r.o[n][1] *= alpha;
-        r.o[n][2] *= alpha;
-        r.o[n][3] *= alpha;
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const bool raise0 = mx0 > r.m[0] + kRescaleLog2, raise1 = mx1 > r.m[1] + kRescaleLog2;
+    if (__any_sync(0xffffffffu, raise0 || raise1)) {
+      const float m0 = raise0 ? mx0 : r.m[0], m1 = raise1 ? mx1 : r.m[1];
+      const float al0 = exp2f(r.m[0] - m0), al1 = exp2f(r.m[1] - m1);  // 0 on the first chunk, 1 if unchanged
+      r.m[0] = m0;
+      r.m[1] = m1;
+      r.l[0] *= al0;
+      r.l[1] *= al1;
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        r.o[i][0] *= al0;
+        r.o[i][2] *= al0;
+        r.o[i][1] *= al1;
+        r.o[i][3] *= al1;
       }
     }
     float pr[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pr[e] = exp2f(x[e] - r.m);
-    r.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
-    const uint32_t hi0 = pack_bf16x2(pr[0], pr[1]);
-    const uint32_t hi1 = pack_bf16x2(pr[2], pr[3]);
-    const uint32_t lo0 = pack_bf16x2(pr[0] - bf16_lo(hi0), pr[1] - bf16_hi(hi0));
-    const uint32_t lo1 = pack_bf16x2(pr[2] - bf16_lo(hi1), pr[3] - bf16_hi(hi1));
-    // ---- O += P V (rows 0..7: hi, rows 8..15: lo)
-    uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
-    if (vlo > 0 || vhi < kChunk) {  // zero V entries of tokens outside the range (they may hold NaN)
-      mask01 = (ok0 ? 0x0000ffffu : 0u) | (ok1 ? 0xffff0000u : 0u);
-      mask23 = (ok2 ? 0x0000ffffu : 0u) | (ok3 ? 0xffff0000u : 0u);
+    for (int e = 0; e < 4; ++e) pr[e] = exp2f(x[e] - r.m[e & 1]);
+    r.l[0] += pr[0] + pr[2];
+    r.l[1] += pr[1] + pr[3];
+    // ---- P^T fragments: pack [token][column] as bf16 pairs, transpose with movmatrix
+    const uint32_t h0 = pack_bf16x2(pr[0], pr[1]);  // token g
+    const uint32_t h1 = pack_bf16x2(pr[2], pr[3]);  // token g + 8
+    const uint32_t l0 = pack_bf16x2(pr[0] - bf16_lo(h0), pr[1] - bf16_hi(h0));
+    const uint32_t l1 = pack_bf16x2(pr[2] - bf16_lo(h1), pr[3] - bf16_hi(h1));
+    uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+    if constexpr (kPaired) {
+      const bool lo_lane = t >= 2;             // columns 4..7
+      bh0 = movmatrix_t(lo_lane ? l0 : h0);
+      bh1 = movmatrix_t(lo_lane ? l1 : h1);
+    } else {
+      bh0 = movmatrix_t(h0);
+      bh1 = movmatrix_t(h1);
+      bl0 = movmatrix_t(l0);
+      bl1 = movmatrix_t(l1);
     }
-    const int vtok = mr + 8 * (mi & 1);
+    // ---- O^T += V^T P^T; V entries of masked tokens are zeroed (they may hold NaN)
+    uint32_t mk01 = 0xffffffffu, mk23 = 0xffffffffu;  // A registers 0/1: tokens 2t, 2t+1; 2/3: 2t+8, 2t+9
+    if (vlo > 0 || vhi < kChunk) {
+      const int k0 = 2 * t;
+      mk01 = (k0 >= vlo && k0 < vhi ? 0x0000ffffu : 0u) | (k0 + 1 >= vlo && k0 + 1 < vhi ? 0xffff0000u : 0u);
+      mk23 = (k0 + 8 >= vlo && k0 + 8 < vhi ? 0x0000ffffu : 0u) | (k0 + 9 >= vlo && k0 + 9 < vhi ? 0xffff0000u : 0u);
+    }
+    const int vtok = mr + 8 * (mi >> 1);       // matrices 0, 1: tokens 0..7; 2, 3: tokens 8..15
 #pragma unroll
-    for (int pair = 0; pair < NT / 2; ++pair) {
-      const int db = 2 * pair + (mi >> 1);
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vb + (db >> 3) * BOX + swz(vtok, db & 7), v0, v1, v2, v3);
-      mma_bf16_16816(r.o[2 * pair], hi0, lo0, hi1, lo1, v0 & mask01, v1 & mask23);
-      mma_bf16_16816(r.o[2 * pair + 1], hi0, lo0, hi1, lo1, v2 & mask01, v3 & mask23);
+    for (int i = 0; i < KS; ++i) {
+      const int db = 2 * i + (mi & 1);         // matrices 0, 2: dims 16i..+7; 1, 3: dims 16i+8..+15
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vb + (db >> 3) * BOX + swz(vtok, db & 7), a0, a1, a2, a3);
+      a0 &= mk01;
+      a1 &= mk01;
+      a2 &= mk23;
+      a3 &= mk23;
+      mma_bf16_16816(r.o[i], a0, a1, a2, a3, bh0, bh1);
+      if constexpr (!kPaired) mma_bf16_16816(r.o[i], a0, a1, a2, a3, bl0, bl1);
     }
   }
 
   __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
     const int g = lane >> 2, t = lane & 3;
-    float lt = r.l;
-    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-    if (g >= G) return;
-    const float inv = 1.f / lt;
+    float lt0 = r.l[0], lt1 = r.l[1];
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
-      *reinterpret_cast<float2*>(dst + g * D + 8 * n + 2 * t) =
-          make_float2((r.o[n][0] + r.o[n][2]) * inv, (r.o[n][1] + r.o[n][3]) * inv);
-    if (ml != nullptr && t == 0) {
-      ml[2 * g] = r.m;
-      ml[2 * g + 1] = lt;
+    for (int off = 4; off < 32; off <<= 1) {
+      lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+      lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+    }
+    if constexpr (kPaired) {  // lane t < 2 holds hi of heads 2t, 2t+1, lane t + 2 their lo
+#pragma unroll
+      for (int i = 0; i < KS; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r.o[i][e] += __shfl_xor_sync(0xffffffffu, r.o[i][e], 2);
+    }
+    const int hd0 = 2 * t, hd1 = 2 * t + 1;
+    const bool w0 = (!kPaired || t < 2) && hd0 < G;
+    const bool w1 = (!kPaired || t < 2) && hd1 < G;
+    const float inv0 = 1.f / lt0, inv1 = 1.f / lt1;
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const int d0 = 16 * i + g;
+      if (w0) {
+        dst[hd0 * D + d0] = r.o[i][0] * inv0;
+        dst[hd0 * D + d0 + 8] = r.o[i][2] * inv0;
+      }
+      if (w1) {
+        dst[hd1 * D + d0] = r.o[i][1] * inv1;
+        dst[hd1 * D + d0 + 8] = r.o[i][3] * inv1;
+      }
+    }
+    if (ml != nullptr && g == 0) {
+      if (w0) {
+        ml[2 * hd0] = r.m[0];
+        ml[2 * hd0 + 1] = lt0;
+      }
+      if (w1) {
+        ml[2 * hd1] = r.m[1];
+        ml[2 * hd1 + 1] = lt1;
+      }
     }
   }
 };
 
 // ------------------------------------------------------------------------------------------------
-// FP8 E4M3 caches (D = 128), G <= 8: f16 tensor-core math on exactly converted codes.
+// FP8 E4M3 caches (D = 128), G <= 8: f16 tensor-core math on exactly converted codes, in the same
+// transposed form as the bf16 path (tokens or dims on the 16-row side, heads on the 8-wide side).
 //
 // Stage: [K box: 16 rows x 128 B, 128-byte swizzle][V box: 128 dims x 16 tokens (V is stored
 // dim-major in fp8 pools)][16 K scales][16 V scales], padded to 5120 bytes.
-// q.K: the contraction over d is order-free, so within each 16-dim k-step lane t takes dims
-// 4t..4t+3 for both operands: ldmatrix on the fp8 rows hands each lane 4 consecutive codes, which
-// cvt turns into the two f16 pairs of its B fragment; q is loaded with the same dim order. p.V: the
-// fp8 V page stores each 16-token group in the order (0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15), so
-// the 4 codes ldmatrix hands lane t from a dim row are tokens (2t, 2t+1, 8+2t, 9+2t): exactly the
-// tokens of lane t's scores and of its P fragment. Per-token scales: S *= k_scale; P' = p * v_scale * 1024 is split
-// into f16 hi + lo (rows 0..7 / 8..15); the running max is raised when a chunk exceeds it by 2^2,
-// so p <= 4 and P' stays inside the f16 normal range for |V| < ~7000.
+// S^T = K q^T: the contraction over d is order-free, so within each 16-dim k-step the fragment's
+// k indices {2t, 2t+1} and {2t+8, 2t+9} stand for dims {4t, 4t+1} and {4t+2, 4t+3}: ldmatrix on the
+// fp8 rows hands lane t the 4 consecutive codes 4t..4t+3, which cvt turns into its two f16 A pairs;
+// q^T is loaded in the same dim order. O^T += V^T P^T: ldmatrix on the dim-major V rows hands lane t
+// stored bytes 4t..4t+3, and the fp8 V page stores each 16-token group in the order
+// (0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15), so those bytes are tokens {2t, 2t+1} and {2t+8, 2t+9}:
+// exactly the k indices of the A fragment. Per-token scales: S *= k_scale; P' = p * v_scale * 1024
+// is carried as f16 hi + lo (paired columns as in the bf16 path); the running max is raised when a
+// chunk exceeds it by 2^2, so p <= 4 and P' stays inside the f16 normal range for |V| < ~7000.
 // ------------------------------------------------------------------------------------------------
 template <int G>
 struct Fp8Math {
@@ -648,16 +719,22 @@ struct Fp8Math {
   static constexpr int kTxBytes = KBOX + VBOX + 2 * kChunk * 4;
   static constexpr int kStageBytes = 5120;
   static constexpr int kMinCtasPerSm = 3;
-  static constexpr int KS = D / 16;
-  static constexpr int NT = D / 8;
+  static constexpr int KS = D / 16;          // k-steps of q.K and m-tiles of p.V
+  static constexpr bool kPaired = G <= 4;
   static constexpr float kRescaleLog2 = 2.f;
+  static constexpr int kQElem = 2;
   static constexpr float kPScale = 1024.f;
 
   struct Regs {
-    uint32_t qa[KS][2];
-    float o[NT][4];
-    float m, l;
+    uint32_t qb[KS][2];  // B fragment of q^T (f16): dims 16ks + {4t, 4t+1} and {4t+2, 4t+3}
+    float o[KS][4];      // O^T: dims 16i + g ([0], [1]) and 16i + g + 8 ([2], [3]); columns 2t, 2t+1
+    float m[2], l[2];
   };
+
+  __device__ static __forceinline__ int head_of(int n) {
+    const int hd = kPaired ? (n & 3) : n;
+    return hd < G ? hd : -1;
+  }
 
   __device__ static void issue(const DecodeArgs& a, const TmaMaps& maps, uint32_t dst, uint32_t bar, int64_t row0,
                                uint64_t policy) {
@@ -672,124 +749,167 @@ struct Fp8Math {
 
   __device__ static void load_q(Regs& r, const DecodeArgs& a, int32_t b, int32_t h, int lane) {
     const int g = lane >> 2, t = lane & 3;
+    const int hd = head_of(g);
     const uint2* qrow = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                       (static_cast<int64_t>(b) * a.Hq + h * G + g) * D);
+                                                       (static_cast<int64_t>(b) * a.Hq + h * G + max(hd, 0)) * D);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      if (g < G) {
+      if (hd >= 0) {
         const uint2 w = __ldg(qrow + 4 * ks + t);   // dims 16ks + 4t .. +3
-        r.qa[ks][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
-        r.qa[ks][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+        r.qb[ks][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+        r.qb[ks][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
       } else {
-        r.qa[ks][0] = r.qa[ks][1] = 0u;
+        r.qb[ks][0] = r.qb[ks][1] = 0u;
       }
     }
   }
 
   __device__ static void reset(Regs& r) {
-    r.m = -INFINITY;
-    r.l = 0.f;
+    r.m[0] = r.m[1] = -INFINITY;
+    r.l[0] = r.l[1] = 0.f;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) r.o[n][0] = r.o[n][1] = r.o[n][2] = r.o[n][3] = 0.f;
+    for (int i = 0; i < KS; ++i) r.o[i][0] = r.o[i][1] = r.o[i][2] = r.o[i][3] = 0.f;
   }
 
   __device__ static void chunk(Regs& r, const unsigned char* stage, int vlo, int vhi, float scale_log2, int lane) {
     const uint32_t kb = smem_addr(stage);
     const uint32_t vb = kb + KBOX;
     const float* scl = reinterpret_cast<const float*>(stage + kScaleOff);
-    const int t = lane & 3;
+    const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, mr = lane & 7;
-    float s[2][4];
+    // ---- S^T = K q^T
+    float se[4] = {0.f, 0.f, 0.f, 0.f}, so[4] = {0.f, 0.f, 0.f, 0.f};
+    const int ktok = mr + 8 * (mi & 1);       // matrices 0, 2: tokens 0..7; 1, 3: tokens 8..15
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      float se[4] = {0.f, 0.f, 0.f, 0.f}, so[4] = {0.f, 0.f, 0.f, 0.f};
-      const int tok = 8 * nt + mr;
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        uint32_t w[4];
-        ldsm_x4(kb + tok * 128 + (((4 * p + mi) ^ (tok & 7)) << 4), w[0], w[1], w[2], w[3]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_f16_16816((j & 1) ? so : se, r.qa[4 * p + j][0], 0u, r.qa[4 * p + j][1], 0u, e4m3x2_to_f16x2(w[j]),
-                        e4m3x2_to_f16x2(w[j] >> 16));
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[nt][e] = se[e] + so[e];
+    for (int p = 0; p < KS / 2; ++p) {
+      const int db = 2 * p + (mi >> 1);       // matrices 0, 1: k-step 2p; 2, 3: k-step 2p + 1
+      uint32_t w0, w1, w2, w3;
+      ldsm_x4(kb + ktok * 128 + ((db ^ (ktok & 7)) << 4), w0, w1, w2, w3);
+      mma_f16_16816(se, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
+                    e4m3x2_to_f16x2(w1 >> 16), r.qb[2 * p][0], r.qb[2 * p][1]);
+      mma_f16_16816(so, e4m3x2_to_f16x2(w2), e4m3x2_to_f16x2(w3), e4m3x2_to_f16x2(w2 >> 16),
+                    e4m3x2_to_f16x2(w3 >> 16), r.qb[2 * p + 1][0], r.qb[2 * p + 1][1]);
     }
-    // this lane's tokens: 2t, 2t+1 (n-tile 0) and 8+2t, 9+2t (n-tile 1)
-    const float2 ksa = *reinterpret_cast<const float2*>(scl + 2 * t);
-    const float2 ksb = *reinterpret_cast<const float2*>(scl + 8 + 2 * t);
-    const float2 vsa = *reinterpret_cast<const float2*>(scl + kChunk + 2 * t);
-    const float2 vsb = *reinterpret_cast<const float2*>(scl + kChunk + 8 + 2 * t);
-    const float4 ksc = make_float4(ksa.x, ksa.y, ksb.x, ksb.y);
-    const float4 vsc = make_float4(vsa.x, vsa.y, vsb.x, vsb.y);
-    const bool ok0 = 2 * t >= vlo && 2 * t < vhi, ok1 = 2 * t + 1 >= vlo && 2 * t + 1 < vhi;
-    const bool ok2 = 8 + 2 * t >= vlo && 8 + 2 * t < vhi, ok3 = 9 + 2 * t >= vlo && 9 + 2 * t < vhi;
+    // ---- online softmax per column over tokens {g, g+8}
+    const bool okg = g >= vlo && g < vhi, okg8 = g + 8 >= vlo && g + 8 < vhi;
+    const float ks0 = scl[g] * scale_log2, ks8 = scl[g + 8] * scale_log2;
     float x[4];
-    x[0] = ok0 ? s[0][0] * ksc.x * scale_log2 : -INFINITY;
-    x[1] = ok1 ? s[0][1] * ksc.y * scale_log2 : -INFINITY;
-    x[2] = ok2 ? s[1][0] * ksc.z * scale_log2 : -INFINITY;
-    x[3] = ok3 ? s[1][1] * ksc.w * scale_log2 : -INFINITY;
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const bool raise = mx > r.m + kRescaleLog2;
-    if (__any_sync(0xffffffffu, raise)) {
-      const float mnew = raise ? mx : r.m;
-      const float alpha = exp2f(r.m - mnew);
-      r.m = mnew;
-      r.l *= alpha;
+    x[0] = okg ? (se[0] + so[0]) * ks0 : -INFINITY;
+    x[1] = okg ? (se[1] + so[1]) * ks0 : -INFINITY;
+    x[2] = okg8 ? (se[2] + so[2]) * ks8 : -INFINITY;
+    x[3] = okg8 ? (se[3] + so[3]) * ks8 : -INFINITY;
+    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        r.o[n][0] *= alpha;
-        r.o[n][1] *= alpha;
-        r.o[n][2] *= alpha;
-        r.o[n][3] *= alpha;
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const bool raise0 = mx0 > r.m[0] + kRescaleLog2, raise1 = mx1 > r.m[1] + kRescaleLog2;
+    if (__any_sync(0xffffffffu, raise0 || raise1)) {
+      const float m0 = raise0 ? mx0 : r.m[0], m1 = raise1 ? mx1 : r.m[1];
+      const float al0 = exp2f(r.m[0] - m0), al1 = exp2f(r.m[1] - m1);
+      r.m[0] = m0;
+      r.m[1] = m1;
+      r.l[0] *= al0;
+      r.l[1] *= al1;
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        r.o[i][0] *= al0;
+        r.o[i][2] *= al0;
+        r.o[i][1] *= al1;
+        r.o[i][3] *= al1;
       }
     }
     float pr[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pr[e] = exp2f(x[e] - r.m);
-    r.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    for (int e = 0; e < 4; ++e) pr[e] = exp2f(x[e] - r.m[e & 1]);
+    r.l[0] += pr[0] + pr[2];
+    r.l[1] += pr[1] + pr[3];
     // a masked token's scale may be garbage (even NaN): select 0 rather than multiply
-    const float p0 = ok0 ? pr[0] * vsc.x * kPScale : 0.f, p1 = ok1 ? pr[1] * vsc.y * kPScale : 0.f;
-    const float p2 = ok2 ? pr[2] * vsc.z * kPScale : 0.f, p3 = ok3 ? pr[3] * vsc.w * kPScale : 0.f;
-    const uint32_t hi0 = pack_f16x2(p0, p1), hi1 = pack_f16x2(p2, p3);
-    const uint32_t lo0 = pack_f16x2(p0 - f16_lo(hi0), p1 - f16_hi(hi0));
-    const uint32_t lo1 = pack_f16x2(p2 - f16_lo(hi1), p3 - f16_hi(hi1));
-    uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
-    if (vlo > 0 || vhi < kChunk) {  // zero V entries of tokens outside the range (they may hold NaN)
-      mask01 = (ok0 ? 0x0000ffffu : 0u) | (ok1 ? 0xffff0000u : 0u);
-      mask23 = (ok2 ? 0x0000ffffu : 0u) | (ok3 ? 0xffff0000u : 0u);
+    const float vs0 = scl[kChunk + g] * kPScale, vs8 = scl[kChunk + g + 8] * kPScale;
+    const float p0 = okg ? pr[0] * vs0 : 0.f, p1 = okg ? pr[1] * vs0 : 0.f;
+    const float p2 = okg8 ? pr[2] * vs8 : 0.f, p3 = okg8 ? pr[3] * vs8 : 0.f;
+    const uint32_t h0 = pack_f16x2(p0, p1), h1 = pack_f16x2(p2, p3);
+    const uint32_t l0 = pack_f16x2(p0 - f16_lo(h0), p1 - f16_hi(h0));
+    const uint32_t l1 = pack_f16x2(p2 - f16_lo(h1), p3 - f16_hi(h1));
+    uint32_t bh0, bh1, bl0 = 0u, bl1 = 0u;
+    if constexpr (kPaired) {
+      const bool lo_lane = t >= 2;
+      bh0 = movmatrix_t(lo_lane ? l0 : h0);
+      bh1 = movmatrix_t(lo_lane ? l1 : h1);
+    } else {
+      bh0 = movmatrix_t(h0);
+      bh1 = movmatrix_t(h1);
+      bl0 = movmatrix_t(l0);
+      bl1 = movmatrix_t(l1);
+    }
+    // ---- O^T += V^T P^T; V entries of masked tokens are zeroed (they may hold NaN)
+    uint32_t mk01 = 0xffffffffu, mk23 = 0xffffffffu;  // A registers 0/1: tokens 2t, 2t+1; 2/3: 2t+8, 2t+9
+    if (vlo > 0 || vhi < kChunk) {
+      const int k0 = 2 * t;
+      mk01 = (k0 >= vlo && k0 < vhi ? 0x0000ffffu : 0u) | (k0 + 1 >= vlo && k0 + 1 < vhi ? 0xffff0000u : 0u);
+      mk23 = (k0 + 8 >= vlo && k0 + 8 < vhi ? 0x0000ffffu : 0u) | (k0 + 9 >= vlo && k0 + 9 < vhi ? 0xffff0000u : 0u);
     }
 #pragma unroll
-    for (int q4 = 0; q4 < NT / 4; ++q4) {
-      uint32_t v[4];
-      ldsm_x4(vb + (8 * (4 * q4 + mi) + mr) * kChunk, v[0], v[1], v[2], v[3]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        mma_f16_16816(r.o[4 * q4 + j], hi0, lo0, hi1, lo1, e4m3x2_to_f16x2(v[j]) & mask01,
-                      e4m3x2_to_f16x2(v[j] >> 16) & mask23);
+    for (int q = 0; q < KS / 2; ++q) {             // 32 dims: m-tiles 2q and 2q + 1
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4(vb + (32 * q + 8 * mi + mr) * kChunk, v0, v1, v2, v3);
+      const uint32_t a0 = e4m3x2_to_f16x2(v0) & mk01, a2 = e4m3x2_to_f16x2(v0 >> 16) & mk23;
+      const uint32_t a1 = e4m3x2_to_f16x2(v1) & mk01, a3 = e4m3x2_to_f16x2(v1 >> 16) & mk23;
+      const uint32_t c0 = e4m3x2_to_f16x2(v2) & mk01, c2 = e4m3x2_to_f16x2(v2 >> 16) & mk23;
+      const uint32_t c1 = e4m3x2_to_f16x2(v3) & mk01, c3 = e4m3x2_to_f16x2(v3 >> 16) & mk23;
+      mma_f16_16816(r.o[2 * q], a0, a1, a2, a3, bh0, bh1);
+      mma_f16_16816(r.o[2 * q + 1], c0, c1, c2, c3, bh0, bh1);
+      if constexpr (!kPaired) {
+        mma_f16_16816(r.o[2 * q], a0, a1, a2, a3, bl0, bl1);
+        mma_f16_16816(r.o[2 * q + 1], c0, c1, c2, c3, bl0, bl1);
+      }
     }
   }
 
   __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
     const int g = lane >> 2, t = lane & 3;
-    float lt = r.l;
-    lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-    lt += __shfl_xor_sync(0xffffffffu, lt, 2);
-    if (g >= G) return;
-    const float inv = 1.f / (lt * kPScale);
+    float lt0 = r.l[0], lt1 = r.l[1];
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
-      *reinterpret_cast<float2*>(dst + g * D + 8 * n + 2 * t) =
-          make_float2((r.o[n][0] + r.o[n][2]) * inv, (r.o[n][1] + r.o[n][3]) * inv);
-    if (ml != nullptr && t == 0) {
-      ml[2 * g] = r.m;
-      ml[2 * g + 1] = lt;
+    for (int off = 4; off < 32; off <<= 1) {
+      lt0 += __shfl_xor_sync(0xffffffffu, lt0, off);
+      lt1 += __shfl_xor_sync(0xffffffffu, lt1, off);
+    }
+    if constexpr (kPaired) {
+#pragma unroll
+      for (int i = 0; i < KS; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) r.o[i][e] += __shfl_xor_sync(0xffffffffu, r.o[i][e], 2);
+    }
+    const int hd0 = 2 * t, hd1 = 2 * t + 1;
+    const bool w0 = (!kPaired || t < 2) && hd0 < G;
+    const bool w1 = (!kPaired || t < 2) && hd1 < G;
+    const float inv0 = 1.f / (lt0 * kPScale), inv1 = 1.f / (lt1 * kPScale);
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const int d0 = 16 * i + g;
+      if (w0) {
+        dst[hd0 * D + d0] = r.o[i][0] * inv0;
+        dst[hd0 * D + d0 + 8] = r.o[i][2] * inv0;
+      }
+      if (w1) {
+        dst[hd1 * D + d0] = r.o[i][1] * inv1;
+        dst[hd1 * D + d0 + 8] = r.o[i][3] * inv1;
+      }
+    }
+    if (ml != nullptr && g == 0) {
+      if (w0) {
+        ml[2 * hd0] = r.m[0];
+        ml[2 * hd0 + 1] = lt0;
+      }
+      if (w1) {
+        ml[2 * hd1] = r.m[1];
+        ml[2 * hd1 + 1] = lt1;
+      }
     }
   }
 };
+
 
 // ------------------------------------------------------------------------------------------------
 // The decode kernel: prefix of chunk counts, even split of the flat chunk list over warps, a
@@ -851,25 +971,39 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   if (n_chunks <= 0) return;
 
   // --- producer (lane 0 issues; the block-table window is spread over the lanes) ---
+  // pf walks the chunks ahead of the consumer; (p_pg, p_sub) = its page in the block table and
+  // chunk within that page, stepped without divisions except at unit changes.
+  const int32_t cpb = a.B / kChunk;
   Cursor pf = locate(pref, n, Hkv, lo);
+  int32_t p_pg = 0, p_sub = 0;
+  auto p_unit_start = [&]() {
+    const int32_t ch = cfirst[pf.b] + pf.c;
+    p_pg = ch / cpb;
+    p_sub = ch - p_pg * cpb;
+    // warm L2 with the unit's queries: load_q reads them when the consumer gets here
+    constexpr int kQLines = (G * D * Math::kQElem + 127) / 128;
+    if (lane < kQLines)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const unsigned char*>(a.q) +
+                                                    ((static_cast<int64_t>(pf.b) * a.Hq + pf.h * G) * D) * Math::kQElem +
+                                                    128 * lane));
+  };
+  p_unit_start();
   int32_t win_b = -1, win_base = 0, win_val = -1;
   const uint64_t policy = policy_evict_first();
   int64_t issued = 0;
 
   auto issue = [&](int stage) {
-    const int32_t tok0 = (cfirst[pf.b] + pf.c) * kChunk;
-    const int32_t pg = tok0 / a.B;
-    if (pf.b != win_b || pg < win_base || pg >= win_base + 32) {
+    if (pf.b != win_b || p_pg < win_base || p_pg >= win_base + 32) {
       win_b = pf.b;
-      win_base = pg;
+      win_base = p_pg;
       const int32_t idx = win_base + lane;
       win_val = idx < a.MB ? __ldg(a.block_tables + static_cast<int64_t>(pf.b) * a.MB + idx) : -1;
     }
-    const int32_t blk = __shfl_sync(0xffffffffu, win_val, pg - win_base);
+    const int32_t blk = __shfl_sync(0xffffffffu, win_val, p_pg - win_base);
     if (lane == 0) {
       const uint32_t bar = smem_addr(bars + stage);
       if (blk >= 0 && blk < a.NB) {
-        const int64_t row0 = (static_cast<int64_t>(blk) * Hkv + pf.h) * a.B + (tok0 - pg * a.B);
+        const int64_t row0 = (static_cast<int64_t>(blk) * Hkv + pf.h) * a.B + p_sub * kChunk;
         fence_proxy_async_smem();
         Math::issue(a, maps, smem_addr(ring + static_cast<size_t>(stage) * SB), bar, row0, policy);
       } else {
@@ -877,8 +1011,17 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
         mbar_arrive(bar);  // completes the phase with no data; the chunk's result is garbage
       }
     }
-    advance(pf, pref, n, Hkv);
     ++issued;
+    if (pf.c + 1 < pf.nch) {
+      ++pf.c;
+      if (++p_sub == cpb) {
+        p_sub = 0;
+        ++p_pg;
+      }
+    } else {
+      advance(pf, pref, n, Hkv);
+      if (issued < n_chunks) p_unit_start();
+    }
   };
 
   for (int s = 0; s < S && issued < n_chunks; ++s) issue(s);
@@ -888,20 +1031,44 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   typename Math::Regs r;
   int32_t seg_c0 = cc.c;
   int seg_idx = 0;
+  int stage = 0;
+  uint32_t phase = 0;
 
   int32_t len_b = clamped_len(a, cc.b);
   Math::load_q(r, a, cc.b, cc.h, lane);
   Math::reset(r);
-  bool pend = false;  // this warp completed a split unit with its last segment: merge it at the end
+
+  // Split units. A segment that ends inside this warp's range (the tail of a unit begun by the
+  // previous warp) is published a few chunks later: its partial is stored at once, and the release
+  // fence and arrival wait until those stores have drained, so the fence costs little. The segment
+  // that ends the range (usually the unit's last one to finish) first checks whether all other
+  // segments are already published; if so it merges at once from its own partial and theirs,
+  // without a release or arrival of its own. Otherwise it publishes and the last arrival merges.
+  constexpr int kPubDelay = 2;
+  bool pub = false;
+  int pub_wait = 0;
+  int32_t pub_b = 0, pub_h = 0, pub_kind = 0;
+  int64_t pub_parts = 0, pub_wf = 0;
+  auto publish = [&]() {
+    fence_acq_rel_gpu();  // this warp's partial stores are visible before the arrival
+    __syncwarp();
+    int last = 0;
+    if (lane == 0)
+      last = arrive_last(a.ws_count + static_cast<int64_t>(pub_b) * Hkv + pub_h, a.tag, pub_parts) ? 1 : 0;
+    if (__shfl_sync(0xffffffffu, last, 0)) {
+      fence_acq_rel_gpu();
+      merge_unit<D, G, false>(a, pub_b, pub_h, pub_parts, pub_wf, pub_kind, lane);
+    }
+    pub = false;
+  };
+  bool pend = false;  // this warp merges a unit after the loop (its registers are free then)
   int32_t pend_b = 0, pend_h = 0, pend_kind = 0;
   int64_t pend_parts = 0, pend_wf = 0;
 
   bool aborted = false;
   int64_t i = 0;
   for (; i < n_chunks; ++i) {
-    const int stage = static_cast<int>(i % S);
-    const uint32_t parity = static_cast<uint32_t>((i / S) & 1);
-    if (!mbar_wait_bounded(smem_addr(bars + stage), parity)) {
+    if (!mbar_wait_bounded(smem_addr(bars + stage), phase)) {
       aborted = true;
       break;
     }
@@ -911,6 +1078,11 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     Math::chunk(r, ring + static_cast<size_t>(stage) * SB, vlo, vhi, a.scale_log2, lane);
     __syncwarp();
     if (issued < n_chunks) issue(stage);
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (pub && --pub_wait == 0) publish();
 
     // segment end: write the whole-unit result or a partial
     const bool unit_end = (cc.c + 1 == cc.nch);
@@ -918,13 +1090,12 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     const bool range_end = (i + 1 == n_chunks);
     if (unit_end || part_end || range_end) {
       const bool complete = (seg_c0 == 0) && unit_end;
-      const int64_t u = static_cast<int64_t>(cc.b) * Hkv + cc.h;
       if (complete) {
         Math::finish(r, a.out + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G) * D, nullptr, lane);
       } else {
+        const int64_t u = static_cast<int64_t>(cc.b) * Hkv + cc.h;
         const int64_t slot = (PC == 0) ? (2 * static_cast<int64_t>(w) + (seg_idx == 0 ? 0 : 1))
                                        : (u * a.max_parts + cc.c / PC);
-        Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
         // Segments of this unit: balanced mode, warps warp_of(s_u) .. warp_of(e_u - 1) where
         // warp_of(p) = floor(((p + 1) * Weff - 1) / NP); fixed mode, its partitions.
         int64_t n_parts, wf = 0;
@@ -938,22 +1109,42 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
         } else {
           n_parts = (cc.nch + PC - 1) / PC;
         }
-        __threadfence();  // this segment's partial is visible before the arrival
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) last = arrive_last(a.ws_count + u, a.tag, n_parts) ? 1 : 0;
-        if (__shfl_sync(0xffffffffu, last, 0)) {
-          __threadfence();
-          if (range_end) {  // the usual case: merge after the loop, when its registers are free
+        if (pub) publish();
+        if (range_end) {
+          int others = 0;
+          if (lane == 0) {
+            const unsigned long long v = ld_acquire_gpu(a.ws_count + u);
+            others = ((v >> 16) == a.tag && static_cast<int64_t>(v & 0xffffull) == n_parts - 1) ? 1 : 0;
+          }
+          others = __shfl_sync(0xffffffffu, others, 0);
+          if (others) fence_acq_rel_gpu();  // the other segments' partials are read after this point
+          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
+          int mine = others;
+          if (!others) {
+            fence_acq_rel_gpu();
+            __syncwarp();
+            if (lane == 0) mine = arrive_last(a.ws_count + u, a.tag, n_parts) ? 1 : 0;
+            mine = __shfl_sync(0xffffffffu, mine, 0);
+            if (mine) fence_acq_rel_gpu();
+          }
+          __syncwarp();  // this warp's own partial is visible to all its lanes
+          if (mine) {
             pend = true;
             pend_b = cc.b;
             pend_h = cc.h;
             pend_parts = n_parts;
             pend_wf = wf;
             pend_kind = first_kind;
-          } else {
-            merge_unit<D, G, false>(a, cc.b, cc.h, n_parts, wf, first_kind, lane);
           }
+        } else {
+          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
+          pub = true;
+          pub_wait = kPubDelay;
+          pub_b = cc.b;
+          pub_h = cc.h;
+          pub_parts = n_parts;
+          pub_wf = wf;
+          pub_kind = first_kind;
         }
       }
       ++seg_idx;
@@ -976,6 +1167,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     for (int64_t k = i + 1; k < issued; ++k)
       mbar_wait_bounded(smem_addr(bars + static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1));
   }
+  if (pub) publish();
   pdl_launch_dependents();
   if (pend) merge_unit<D, G, true>(a, pend_b, pend_h, pend_parts, pend_wf, pend_kind, lane);
 }

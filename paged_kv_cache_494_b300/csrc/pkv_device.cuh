@@ -129,6 +129,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements spread over the warp in mma fragment order (lane
+// 4r + c holds row r, columns 2c and 2c + 1): afterwards lane 4r + c holds row r of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // D = A(16x16, bf16, row) * B(16x8, bf16, col) + D, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
