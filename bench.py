@@ -155,9 +155,9 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def decode_traffic_record():
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary, if the kernel
-    source it was taken on is unchanged (else None)."""
+def decode_traffic_record(workload: str):
+    """Per-launch DRAM bytes of the decode kernel on `workload` from the committed ncu summary, if
+    the kernel source it was taken on is unchanged (else None)."""
     rec = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(rec):
         return None
@@ -165,7 +165,7 @@ def decode_traffic_record():
         d = json.load(f)
     if d.get("kernel_sha256") != kernel_sha():
         return None
-    return d
+    return d.get("workloads", {}).get(workload)
 
 
 def kernel_sha() -> str:
@@ -322,7 +322,7 @@ def bench_cuda(args, world, rank, local):
     peak, peak_kind = measured_peaks()
 
     e2e = bench_e2e(s, args, dist, device) if not fp8 else None
-    traffic = decode_traffic_record()
+    traffic = decode_traffic_record(args.workload)
     clk = clocks.summary()
     line = {
         "metric": METRIC,
@@ -351,7 +351,8 @@ def bench_cuda(args, world, rank, local):
         "seq_steps_per_s": round(seq_steps_all / (t_ms_max * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * value / (peak * world), 2),
         "roofline": {
-            "bound": "hbm", "kernel": "paged_decode (decode + log-sum-exp reduce, one pkv_paged_decode call)",
+            "bound": "hbm",
+            "kernel": "paged_decode_kernel (one pkv_paged_decode call; split units merged in-kernel by log-sum-exp)",
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": None if traffic is None else int(traffic["bytes_per_launch_profile"] * dec_bytes_per_launch
@@ -366,7 +367,6 @@ def bench_cuda(args, world, rank, local):
     if fp8:
         line["metric"] = "paged-decode KV GB/s read (fp8 pool, codes + scales); decode seq-steps/sec"
         line.pop("e2e")
-        line["roofline"]["traffic"] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         line["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_seconds)
     if rank == 0:

@@ -60,6 +60,7 @@ struct DecodeArgs {
   int32_t stages;                // ring depth per warp
   int32_t total_warps;           // warps of the decode grid (balanced-mode slot count / 2)
   int32_t window;                // > 0: attend only to the last `window` positions (sliding window)
+  int32_t min_chunks;            // balanced mode: at least this many chunks per warp (fewer, longer ranges)
   float scale_log2;              // scale * log2(e)
   const float* k_scale;          // fp8 pools: [NB][Hkv][B] per-(token, head) scales (else unused)
   const float* v_scale;
@@ -954,9 +955,13 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     for (int i = lane; i < a.Hq * D / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  // Balanced mode splits the chunks over Weff = min(W, NP) warps so that every range between a
-  // unit's first and last warp is non-empty (the merge relies on it).
-  const int64_t Weff = NP < W ? NP : W;
+  // Balanced mode splits the chunks over Weff = min(W, max(1, NP / mc)) warps, mc = min_chunks (half
+  // of it below 8192 chunks in all): every range is non-empty (the merge relies on it) and problems
+  // are not cut into slivers whose fixed costs (first copy latency, partial writes, merges of many
+  // parts) outweigh their work.
+  const int64_t mc = NP < 8192 ? (a.min_chunks + 1) / 2 : a.min_chunks;  // small problems: shorter ranges
+  const int64_t Wmax = NP / mc > 0 ? NP / mc : 1;
+  const int64_t Weff = Wmax < W ? Wmax : W;
   int64_t lo, hi;
   if (PC == 0) {
     if (w >= Weff) return;

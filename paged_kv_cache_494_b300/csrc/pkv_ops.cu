@@ -226,6 +226,38 @@ bool ensure_smem(const void* fn, size_t bytes) {
   return true;
 }
 
+// Resident CTAs per SM of a kernel at a block size and dynamic shared-memory size, looked up once
+// per (device, kernel, block, smem): the occupancy query is the costliest host step of a launch.
+int occupancy(const void* fn, int threads, size_t smem) {
+  struct Key {
+    int dev;
+    const void* fn;
+    int threads;
+    size_t smem;
+    bool operator==(const Key& o) const { return dev == o.dev && fn == o.fn && threads == o.threads && smem == o.smem; }
+  };
+  struct KeyHash {
+    size_t operator()(const Key& k) const {
+      return std::hash<const void*>()(k.fn) ^ (static_cast<size_t>(k.dev) << 48) ^
+             (static_cast<size_t>(k.threads) << 32) ^ k.smem;
+    }
+  };
+  static std::mutex mu;
+  static std::unordered_map<Key, int, KeyHash> cache;
+  Key key{0, fn, threads, smem};
+  if (cudaGetDevice(&key.dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = per_sm;
+  return per_sm;
+}
+
 struct DecodePlan {
   KernelPair k;
   int nw = 4, stages = 2, grid = 0, warps = 0;
@@ -263,9 +295,7 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   pl.stages = env_int("PKV_DECODE_STAGES", 2);
   pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.stage_bytes, n_seqs);
   if (!ensure_smem(reinterpret_cast<const void*>(pl.k.decode), pl.smem)) return PKV_ERR_CUDA;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pl.k.decode, pl.nw * 32, pl.smem) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  const int per_sm = occupancy(reinterpret_cast<const void*>(pl.k.decode), pl.nw * 32, pl.smem);
   const int sms = num_sms();
   if (per_sm <= 0 || sms <= 0) return PKV_ERR_CUDA;
   pl.grid = sms * per_sm;
@@ -567,6 +597,11 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   }
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  // Balanced mode gives every warp at least 16 chunks (256 tokens), 8 when the whole call has fewer
+  // than 8192 chunks: below that, cutting units into more parts costs more in merges than the extra
+  // warps gain (measured on batches of 4-256 sequences of 256-4096 tokens; problems with more than
+  // 16 chunks per warp are unaffected).
+  a.min_chunks = env_int("PKV_DECODE_MIN_CHUNKS", 16);
   a.tag = next_call_tag();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||

@@ -115,6 +115,14 @@ def test_workspace_reused_by_consecutive_calls_bitwise(path):
         assert torch.equal(run(pt, n, ws), fresh[(pt, n)]), (it, pt, n)
 
 
+@pytest.mark.parametrize("name", ["tiny_f32", "gqa5_bf16", "prefix_cow_partial_bf16"])
+def test_many_way_splits(name, monkeypatch):
+    """One chunk per warp at least (PKV_DECODE_MIN_CHUNKS=1): units cut into dozens of parts."""
+    monkeypatch.setenv("PKV_DECODE_MIN_CHUNKS", "1")
+    c = case_from_workload(name)
+    check(c, c.gpu_decode(0))
+
+
 def test_shared_prefix_equals_duplicated_bitwise():
     """Same logical data: prefix pages shared through forks vs private copies written separately."""
     B, H, D = 16, 8, 128
@@ -136,7 +144,9 @@ def test_shared_prefix_equals_duplicated_bitwise():
     a = shared.gpu_decode(q=q, tables=torch.from_numpy(tables).cuda(), lens=lens_d)
     b = shared.gpu_decode(q=q, tables=torch.from_numpy(dup_tables).cuda(), lens=lens_d)
     assert torch.equal(a, b)
-    assert torch.equal(a[0], a[1])
+    # the two rows hold the same data at different batch positions; the balanced split may cut their
+    # units differently, so they agree to rounding, not bitwise
+    assert float((a[0] - a[1]).abs().max()) <= 1e-5
 
 
 def test_decode_steps_append_then_attend(path):
