@@ -343,6 +343,7 @@ struct SimtMath {
   static constexpr int kStageBytes = 2 * CB;
   static constexpr int kMinCtasPerSm = 1;     // register-heavy: let the compiler use up to 255
   static constexpr int kQElem = es;
+  static constexpr bool kMaskVariants = false;  // one chunk routine checks the token range itself
   static_assert(LPT * EPL == D && TPP * LPT == 32 && PASSES * TPP == kChunk, "lane layout");
   static_assert(PIECES * PER16 == EPL, "pieces");
 
@@ -387,6 +388,7 @@ struct SimtMath {
   }
 
   // Tokens vlo <= tok < vhi of the chunk are inside the attention range; the rest are masked.
+  template <bool kMask>
   __device__ static void chunk(Regs& r, const unsigned char* kb, int vlo, int vhi, float, int lane) {
     const unsigned char* vb = kb + CB;
     const int tg = lane / LPT;
@@ -512,6 +514,7 @@ struct MmaMath {
   static constexpr bool kPaired = G <= 4;    // columns 4..7 repeat heads 0..3 and carry lo
   static constexpr float kRescaleLog2 = 8.f;
   static constexpr int kQElem = 2;
+  static constexpr bool kMaskVariants = true;   // full chunks skip the masking work
 
   struct Regs {
     uint32_t qb[KS][2];  // B fragment of q^T: head of column g, dims 16ks + {2t, 2t+1} and {+8, +9}
@@ -561,6 +564,7 @@ struct MmaMath {
   }
 
   // Tokens vlo <= tok < vhi of the chunk are inside the attention range; the rest are masked.
+  template <bool kMask>  // kMask: some tokens of the chunk lie outside [vlo, vhi)
   __device__ static void chunk(Regs& r, const unsigned char* kbase, int vlo, int vhi, float scale_log2, int lane) {
     const uint32_t kb = smem_addr(kbase);
     const uint32_t vb = kb + CB;
@@ -580,7 +584,7 @@ struct MmaMath {
         mma_bf16_16816(se, a0, a1, a2, a3, r.qb[ks][0], r.qb[ks][1]);
     }
     // ---- online softmax per column over tokens {g, g+8} of every lane
-    const bool okg = g >= vlo && g < vhi, okg8 = g + 8 >= vlo && g + 8 < vhi;
+    const bool okg = !kMask || (g >= vlo && g < vhi), okg8 = !kMask || (g + 8 >= vlo && g + 8 < vhi);
     float x[4];
     x[0] = okg ? (se[0] + so[0]) * scale_log2 : -INFINITY;
     x[1] = okg ? (se[1] + so[1]) * scale_log2 : -INFINITY;
@@ -631,7 +635,7 @@ struct MmaMath {
     }
     // ---- O^T += V^T P^T; V entries of masked tokens are zeroed (they may hold NaN)
     uint32_t mk01 = 0xffffffffu, mk23 = 0xffffffffu;  // A registers 0/1: tokens 2t, 2t+1; 2/3: 2t+8, 2t+9
-    if (vlo > 0 || vhi < kChunk) {
+    if constexpr (kMask) {
       const int k0 = 2 * t;
       mk01 = (k0 >= vlo && k0 < vhi ? 0x0000ffffu : 0u) | (k0 + 1 >= vlo && k0 + 1 < vhi ? 0xffff0000u : 0u);
       mk23 = (k0 + 8 >= vlo && k0 + 8 < vhi ? 0x0000ffffu : 0u) | (k0 + 9 >= vlo && k0 + 9 < vhi ? 0xffff0000u : 0u);
@@ -642,10 +646,12 @@ struct MmaMath {
       const int db = 2 * i + (mi & 1);         // matrices 0, 2: dims 16i..+7; 1, 3: dims 16i+8..+15
       uint32_t a0, a1, a2, a3;
       ldsm_x4_t(vb + (db >> 3) * BOX + swz(vtok, db & 7), a0, a1, a2, a3);
-      a0 &= mk01;
-      a1 &= mk01;
-      a2 &= mk23;
-      a3 &= mk23;
+      if constexpr (kMask) {
+        a0 &= mk01;
+        a1 &= mk01;
+        a2 &= mk23;
+        a3 &= mk23;
+      }
       mma_bf16_16816(r.o[i], a0, a1, a2, a3, bh0, bh1);
       if constexpr (!kPaired) mma_bf16_16816(r.o[i], a0, a1, a2, a3, bl0, bl1);
     }
@@ -724,6 +730,7 @@ struct Fp8Math {
   static constexpr bool kPaired = G <= 4;
   static constexpr float kRescaleLog2 = 2.f;
   static constexpr int kQElem = 2;
+  static constexpr bool kMaskVariants = true;
   static constexpr float kPScale = 1024.f;
 
   struct Regs {
@@ -772,6 +779,7 @@ struct Fp8Math {
     for (int i = 0; i < KS; ++i) r.o[i][0] = r.o[i][1] = r.o[i][2] = r.o[i][3] = 0.f;
   }
 
+  template <bool kMask>  // kMask: some tokens of the chunk lie outside [vlo, vhi)
   __device__ static void chunk(Regs& r, const unsigned char* stage, int vlo, int vhi, float scale_log2, int lane) {
     const uint32_t kb = smem_addr(stage);
     const uint32_t vb = kb + KBOX;
@@ -786,13 +794,16 @@ struct Fp8Math {
       const int db = 2 * p + (mi >> 1);       // matrices 0, 1: k-step 2p; 2, 3: k-step 2p + 1
       uint32_t w0, w1, w2, w3;
       ldsm_x4(kb + ktok * 128 + ((db ^ (ktok & 7)) << 4), w0, w1, w2, w3);
-      mma_f16_16816(se, e4m3x2_to_f16x2(w0), e4m3x2_to_f16x2(w1), e4m3x2_to_f16x2(w0 >> 16),
-                    e4m3x2_to_f16x2(w1 >> 16), r.qb[2 * p][0], r.qb[2 * p][1]);
-      mma_f16_16816(so, e4m3x2_to_f16x2(w2), e4m3x2_to_f16x2(w3), e4m3x2_to_f16x2(w2 >> 16),
-                    e4m3x2_to_f16x2(w3 >> 16), r.qb[2 * p + 1][0], r.qb[2 * p + 1][1]);
+      uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+      e4m3x4_to_f16x2x2(w0, a0, a2);
+      e4m3x4_to_f16x2x2(w1, a1, a3);
+      e4m3x4_to_f16x2x2(w2, c0, c2);
+      e4m3x4_to_f16x2x2(w3, c1, c3);
+      mma_f16_16816(se, a0, a1, a2, a3, r.qb[2 * p][0], r.qb[2 * p][1]);
+      mma_f16_16816(so, c0, c1, c2, c3, r.qb[2 * p + 1][0], r.qb[2 * p + 1][1]);
     }
     // ---- online softmax per column over tokens {g, g+8}
-    const bool okg = g >= vlo && g < vhi, okg8 = g + 8 >= vlo && g + 8 < vhi;
+    const bool okg = !kMask || (g >= vlo && g < vhi), okg8 = !kMask || (g + 8 >= vlo && g + 8 < vhi);
     const float ks0 = scl[g] * scale_log2, ks8 = scl[g + 8] * scale_log2;
     float x[4];
     x[0] = okg ? (se[0] + so[0]) * ks0 : -INFINITY;
@@ -846,7 +857,7 @@ struct Fp8Math {
     }
     // ---- O^T += V^T P^T; V entries of masked tokens are zeroed (they may hold NaN)
     uint32_t mk01 = 0xffffffffu, mk23 = 0xffffffffu;  // A registers 0/1: tokens 2t, 2t+1; 2/3: 2t+8, 2t+9
-    if (vlo > 0 || vhi < kChunk) {
+    if constexpr (kMask) {
       const int k0 = 2 * t;
       mk01 = (k0 >= vlo && k0 < vhi ? 0x0000ffffu : 0u) | (k0 + 1 >= vlo && k0 + 1 < vhi ? 0xffff0000u : 0u);
       mk23 = (k0 + 8 >= vlo && k0 + 8 < vhi ? 0x0000ffffu : 0u) | (k0 + 9 >= vlo && k0 + 9 < vhi ? 0xffff0000u : 0u);
@@ -855,10 +866,21 @@ struct Fp8Math {
     for (int q = 0; q < KS / 2; ++q) {             // 32 dims: m-tiles 2q and 2q + 1
       uint32_t v0, v1, v2, v3;
       ldsm_x4(vb + (32 * q + 8 * mi + mr) * kChunk, v0, v1, v2, v3);
-      const uint32_t a0 = e4m3x2_to_f16x2(v0) & mk01, a2 = e4m3x2_to_f16x2(v0 >> 16) & mk23;
-      const uint32_t a1 = e4m3x2_to_f16x2(v1) & mk01, a3 = e4m3x2_to_f16x2(v1 >> 16) & mk23;
-      const uint32_t c0 = e4m3x2_to_f16x2(v2) & mk01, c2 = e4m3x2_to_f16x2(v2 >> 16) & mk23;
-      const uint32_t c1 = e4m3x2_to_f16x2(v3) & mk01, c3 = e4m3x2_to_f16x2(v3 >> 16) & mk23;
+      uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+      e4m3x4_to_f16x2x2(v0, a0, a2);
+      e4m3x4_to_f16x2x2(v1, a1, a3);
+      e4m3x4_to_f16x2x2(v2, c0, c2);
+      e4m3x4_to_f16x2x2(v3, c1, c3);
+      if constexpr (kMask) {
+        a0 &= mk01;
+        a1 &= mk01;
+        c0 &= mk01;
+        c1 &= mk01;
+        a2 &= mk23;
+        a3 &= mk23;
+        c2 &= mk23;
+        c3 &= mk23;
+      }
       mma_f16_16816(r.o[2 * q], a0, a1, a2, a3, bh0, bh1);
       mma_f16_16816(r.o[2 * q + 1], c0, c1, c2, c3, bh0, bh1);
       if constexpr (!kPaired) {
@@ -1080,7 +1102,10 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     const int32_t tok_abs = (cfirst[cc.b] + cc.c) * kChunk;
     const int32_t vhi = min(kChunk, len_b - tok_abs);
     const int32_t vlo = a.window > 0 ? max(0, len_b - a.window - tok_abs) : 0;
-    Math::chunk(r, ring + static_cast<size_t>(stage) * SB, vlo, vhi, a.scale_log2, lane);
+    if (!Math::kMaskVariants || vlo > 0 || vhi < kChunk)
+      Math::template chunk<true>(r, ring + static_cast<size_t>(stage) * SB, vlo, vhi, a.scale_log2, lane);
+    else
+      Math::template chunk<false>(r, ring + static_cast<size_t>(stage) * SB, vlo, vhi, a.scale_log2, lane);
     __syncwarp();
     if (issued < n_chunks) issue(stage);
     if (++stage == S) {

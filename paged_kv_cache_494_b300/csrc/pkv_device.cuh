@@ -182,6 +182,14 @@ __device__ __forceinline__ float f16_hi(uint32_t w) {
 }
 
 // Two FP8 E4M3 codes (low byte first) -> packed f16 pair (exact: every E4M3 value is an f16).
+// Four E4M3 codes (bytes 0..3 of w) -> two f16x2: lo = codes 0, 1; hi = codes 2, 3 (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t r;
   const uint16_t c = static_cast<uint16_t>(two_codes & 0xffffu);
