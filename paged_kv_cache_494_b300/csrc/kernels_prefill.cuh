@@ -238,20 +238,28 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(const __grid_constan
     if (warp_has_rows) {
       const uint32_t kb = smem_addr(ring + static_cast<size_t>(stage) * SB);
       const uint32_t vb = kb + CB;
-      float s[2][4];
+      // four independent accumulation chains: (n-tile, even / odd k-step)
+      float se[2][4], so[2][4], s[2][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        const int tok = 8 * nt + mr;
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int p = 0; p < KS / 2; ++p) {
+        for (int e = 0; e < 4; ++e) se[nt][e] = so[nt][e] = 0.f;
+#pragma unroll
+      for (int p = 0; p < KS / 2; ++p) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int tok = 8 * nt + mr;
           const int db = 4 * p + mi;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + (db >> 3) * BOX + prefill_swz(tok, db & 7), b0, b1, b2, b3);
-          mma_bf16_16816(s[nt], qa[2 * p][0], qa[2 * p][1], qa[2 * p][2], qa[2 * p][3], b0, b1);
-          mma_bf16_16816(s[nt], qa[2 * p + 1][0], qa[2 * p + 1][1], qa[2 * p + 1][2], qa[2 * p + 1][3], b2, b3);
+          mma_bf16_16816(se[nt], qa[2 * p][0], qa[2 * p][1], qa[2 * p][2], qa[2 * p][3], b0, b1);
+          mma_bf16_16816(so[nt], qa[2 * p + 1][0], qa[2 * p + 1][1], qa[2 * p + 1][2], qa[2 * p + 1][3], b2, b3);
         }
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[nt][e] = se[nt][e] + so[nt][e];
       // keys of this lane: cpos + {2t, 2t+1, 8+2t, 9+2t}; rows g (k = 0, accum [0..1]) and g+8 ([2..3])
       const int kk[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
       float pr[2][4];
@@ -292,8 +300,9 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(const __grid_constan
       const uint32_t l2 = pack_bf16x2(pr[0][2] - bf16_lo(h2), pr[0][3] - bf16_hi(h2));
       const uint32_t l3 = pack_bf16x2(pr[1][2] - bf16_lo(h3), pr[1][3] - bf16_hi(h3));
       // keys at or past the context end may hold garbage (even NaN): zero their V entries
+      const bool tail = cpos + kChunk > len;
       uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
-      if (cpos + kChunk > len) {
+      if (tail) {
         mask01 = ((cpos + 2 * t < len) ? 0x0000ffffu : 0u) | ((cpos + 2 * t + 1 < len) ? 0xffff0000u : 0u);
         mask23 = ((cpos + 8 + 2 * t < len) ? 0x0000ffffu : 0u) | ((cpos + 9 + 2 * t < len) ? 0xffff0000u : 0u);
       }
@@ -303,10 +312,12 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(const __grid_constan
         const int db = 2 * pair + (mi >> 1);
         uint32_t v0, v1, v2, v3;
         ldsm_x4_t(vb + (db >> 3) * BOX + prefill_swz(vtok, db & 7), v0, v1, v2, v3);
-        v0 &= mask01;
-        v1 &= mask23;
-        v2 &= mask01;
-        v3 &= mask23;
+        if (tail) {
+          v0 &= mask01;
+          v1 &= mask23;
+          v2 &= mask01;
+          v3 &= mask23;
+        }
         mma_bf16_16816(o[2 * pair], h0, h1, h2, h3, v0, v1);
         mma_bf16_16816(o[2 * pair], l0, l1, l2, l3, v0, v1);
         mma_bf16_16816(o[2 * pair + 1], h0, h1, h2, h3, v2, v3);
