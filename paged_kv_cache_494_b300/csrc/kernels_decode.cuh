@@ -80,6 +80,7 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long
   return v;
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void fence_acq_rel_cta() { asm volatile("fence.acq_rel.cta;" ::: "memory"); }
 
 __device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned long long tag, int64_t n_parts) {
   unsigned long long old = ld_relaxed_gpu(ctr), assumed, next;
@@ -95,7 +96,15 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned lo
 // 2 * (wf + k) + (k == 0 ? first_kind : 0) in balanced mode (part_chunks == 0), else
 // u * max_parts + k. kWide loads all of a segment's values before combining them (more registers,
 // one memory latency per segment); the narrow form works through them one float4 at a time.
-template <int D, int G, bool kWide>
+// Loads of published partials: from L2 when other SMs wrote them (their stores do not update this
+// SM's L1), through L1 when this CTA's own warps did (CTA-scope ordering).
+template <bool kCta, class T>
+__device__ __forceinline__ T ld_part(const T* p) {
+  if constexpr (kCta) return *p;
+  else return __ldcg(p);
+}
+
+template <int D, int G, bool kWide, bool kCta>
 __device__ __noinline__ void merge_unit(const DecodeArgs& a, int32_t b, int32_t h, int64_t n_parts, int64_t wf,
                                         int first_kind, int lane) {
   const int64_t u = static_cast<int64_t>(b) * a.Hkv + h;
@@ -113,8 +122,8 @@ __device__ __noinline__ void merge_unit(const DecodeArgs& a, int32_t b, int32_t 
 #pragma unroll 1
       for (int64_t k = 0; k < n_parts; ++k) {
         const int64_t sl = slot_of(k);
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (sl * G + j) * 2));
-        const float4 o = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (sl * G + j) * D) + (idx - j * (D / 4)));
+        const float2 ml = ld_part<kCta>(reinterpret_cast<const float2*>(a.ws_ml + (sl * G + j) * 2));
+        const float4 o = ld_part<kCta>(reinterpret_cast<const float4*>(a.ws_o + (sl * G + j) * D) + (idx - j * (D / 4)));
         const float Mn = fmaxf(M, ml.x);
         const float c = exp2f(M - Mn);
         const float wk = ml.y * exp2f(ml.x - Mn);
@@ -149,8 +158,8 @@ __device__ __noinline__ void merge_unit(const DecodeArgs& a, int32_t b, int32_t 
       const int idx = lane + 32 * r;
       if (idx < V4) {
         const int j = idx / (D / 4);
-        ml[r] = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2));
-        o[r] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D) + (idx - j * (D / 4)));
+        ml[r] = ld_part<kCta>(reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2));
+        o[r] = ld_part<kCta>(reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D) + (idx - j * (D / 4)));
       }
     }
 #pragma unroll
@@ -958,6 +967,11 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   int32_t* ipref = pref + (n + 1);
   int32_t* cfirst = ipref + (n + 1);
 
+  // Arrival counters of split units whose segments all belong to this CTA, indexed by the unit's
+  // first warp within the CTA (a warp is the first warp of at most one split unit). wsum[16..24) is
+  // not used by the prefix build; the barrier after it orders the zeroing before any arrival.
+  int32_t* cta_cnt = wsum + 16;
+  if (threadIdx.x < NW) cta_cnt[threadIdx.x] = 0;
   pdl_wait();
   build_prefix(a, pref, ipref, cfirst, wsum);
   if (lane == 0) {
@@ -1076,19 +1090,24 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   int pub_wait = 0;
   int32_t pub_b = 0, pub_h = 0, pub_kind = 0;
   int64_t pub_parts = 0, pub_wf = 0;
+  // Release / acquire around an arrival (memory-model order): every lane's partial stores, then the
+  // warp barrier, then the release fence and lane 0's atomic; on the last arrival, the acquire fence
+  // and a warp barrier before any lane reads the other segments' partials.
   auto publish = [&]() {
-    fence_acq_rel_gpu();  // this warp's partial stores are visible before the arrival
     __syncwarp();
+    fence_acq_rel_gpu();  // this warp's partial stores are visible before the arrival
     int last = 0;
     if (lane == 0)
       last = arrive_last(a.ws_count + static_cast<int64_t>(pub_b) * Hkv + pub_h, a.tag, pub_parts) ? 1 : 0;
     if (__shfl_sync(0xffffffffu, last, 0)) {
       fence_acq_rel_gpu();
-      merge_unit<D, G, false>(a, pub_b, pub_h, pub_parts, pub_wf, pub_kind, lane);
+      __syncwarp();
+      merge_unit<D, G, false, false>(a, pub_b, pub_h, pub_parts, pub_wf, pub_kind, lane);
     }
     pub = false;
   };
   bool pend = false;  // this warp merges a unit after the loop (its registers are free then)
+  bool pend_cta = false;  // ... whose segments all belong to this CTA
   int32_t pend_b = 0, pend_h = 0, pend_kind = 0;
   int64_t pend_parts = 0, pend_wf = 0;
 
@@ -1139,8 +1158,31 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
         } else {
           n_parts = (cc.nch + PC - 1) / PC;
         }
+        const bool intra = (PC == 0) && (wf / NW == (wf + n_parts - 1) / NW);
         if (pub) publish();
-        if (range_end) {
+        if (intra) {
+          // all segments in this CTA: CTA-scope release / acquire around a shared-memory count
+          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
+          __syncwarp();
+          fence_acq_rel_cta();
+          int last = 0;
+          if (lane == 0) last = (atomicAdd(cta_cnt + (wf % NW), 1) + 1 == n_parts) ? 1 : 0;
+          if (__shfl_sync(0xffffffffu, last, 0)) {
+            fence_acq_rel_cta();
+            __syncwarp();
+            if (range_end) {
+              pend = true;
+              pend_cta = true;
+              pend_b = cc.b;
+              pend_h = cc.h;
+              pend_parts = n_parts;
+              pend_wf = wf;
+              pend_kind = first_kind;
+            } else {
+              merge_unit<D, G, false, true>(a, cc.b, cc.h, n_parts, wf, first_kind, lane);
+            }
+          }
+        } else if (range_end) {
           int others = 0;
           if (lane == 0) {
             const unsigned long long v = ld_acquire_gpu(a.ws_count + u);
@@ -1151,8 +1193,8 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
           Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
           int mine = others;
           if (!others) {
-            fence_acq_rel_gpu();
             __syncwarp();
+            fence_acq_rel_gpu();
             if (lane == 0) mine = arrive_last(a.ws_count + u, a.tag, n_parts) ? 1 : 0;
             mine = __shfl_sync(0xffffffffu, mine, 0);
             if (mine) fence_acq_rel_gpu();
@@ -1199,7 +1241,12 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   }
   if (pub) publish();
   pdl_launch_dependents();
-  if (pend) merge_unit<D, G, true>(a, pend_b, pend_h, pend_parts, pend_wf, pend_kind, lane);
+  if (pend) {
+    if (pend_cta)
+      merge_unit<D, G, true, true>(a, pend_b, pend_h, pend_parts, pend_wf, pend_kind, lane);
+    else
+      merge_unit<D, G, true, false>(a, pend_b, pend_h, pend_parts, pend_wf, pend_kind, lane);
+  }
 }
 
 }  // namespace pkv_dev
