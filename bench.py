@@ -168,13 +168,37 @@ def decode_traffic_record(workload: str):
     return d.get("workloads", {}).get(workload)
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without // and /* */ comments or trailing blanks (comment edits keep the hash)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif src[i] == '"':                      # string literal (asm text): copied verbatim
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(src[i])
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+
+
 def kernel_sha() -> str:
+    """Hash of the kernel sources' code (comments excluded): identifies the kernels ncu counters
+    were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_494_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()
 
 

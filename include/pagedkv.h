@@ -229,9 +229,10 @@ PKV_API pkv_status pkv_copy_blocks(const pkv_pool* pool, void* const* k_caches, 
  * block_tables: int32 [n_seqs][max_blocks_per_seq]; context_lens: int32 [n_seqs], each at most
  * max_blocks_per_seq * B.
  * partition_tokens = 0: the library splits the total work evenly over the GPU (whole 16-token
- * chunks) and merges split sequences with a log-sum-exp reduce. partition_tokens > 0 (a multiple
- * of 16): every sequence is cut into partitions of that many tokens, each computed separately and
- * merged by the same reduce. The result never depends on where blocks are placed physically.
+ * chunks) and merges the parts of split sequences by log-sum-exp inside the same kernel.
+ * partition_tokens > 0 (a multiple of 16): every sequence is cut into partitions of that many
+ * tokens, each computed separately and merged the same way. The result never depends on where
+ * blocks are placed physically (it may depend, to rounding, on a sequence's batch position).
  * workspace: device scratch of at least pkv_decode_workspace_bytes(...) bytes (may be NULL if that
  * is 0); its contents need no initialisation. Concurrent calls must not share a workspace. */
 PKV_API pkv_status pkv_paged_decode(const pkv_pool* pool, float* out, const void* q, const void* k_cache,

@@ -1,4 +1,4 @@
-// Paged decode attention (K3) and its log-sum-exp merge (K4 reduce).
+// Paged decode attention (K3) and the log-sum-exp merge of split sequences (K4), in one kernel.
 //
 // What is computed ("Servicio de modelos de lenguaje con un presupuesto de memoria" §6): for each
 // sequence b and query head j, out = softmax(scale * q K^T) V over the sequence's first len_b
@@ -17,15 +17,17 @@
 //  * Per warp, a ring of `stages` shared-memory slots is filled by TMA copies that complete on an
 //    mbarrier; lane 0 issues them `stages` chunks ahead of the compute. The bf16 path uses 2-D
 //    tensor copies with 128-byte swizzle (16 rows x 128 bytes per box) so that ldmatrix reads are
-//    free of bank conflicts, and computes q.K and p.V with mma.sync (m16n8k16, fp32 accumulate);
-//    the fp32 path uses 1-D bulk copies and CUDA-core dot products with warp shuffles.
+//    free of bank conflicts, and computes S^T = K q^T and O^T = V^T P^T with mma.sync (m16n8k16,
+//    fp32 accumulate); the fp32 path uses 1-D bulk copies and CUDA-core dot products.
 //  * A segment is the part of a unit one warp processes. A segment that is a whole unit writes the
 //    output directly; otherwise it writes (m, l, o/l) to the workspace and arrives on the unit's
 //    counter; the warp that arrives last merges the unit's segments: M = max m_k,
 //    w_k = l_k 2^(m_k - M), o = sum w_k o_k / sum w_k. m is kept in log2 units (scores
-//    pre-multiplied by scale * log2 e), which changes no result. Counters carry a tag unique to the
-//    call in their high 48 bits, so they never need clearing: a count left by an earlier call (or
-//    never written) carries another tag and restarts at 1.
+//    pre-multiplied by scale * log2 e), which changes no result. Units whose segments all lie in
+//    one CTA count arrivals in shared memory under CTA-scope fences; the others use global
+//    counters under GPU-scope fences. Global counters carry a tag unique to the call in their high
+//    48 bits, so they never need clearing: a count left by an earlier call (or never written)
+//    carries another tag and restarts at 1.
 //  * The split depends only on the context lengths, never on physical block ids, so results are
 //    bitwise invariant under any placement of the blocks.
 #pragma once
