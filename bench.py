@@ -169,7 +169,8 @@ def decode_traffic_record(workload: str):
 
 
 def _strip_comments(src: str) -> str:
-    """C/C++ source without // and /* */ comments or trailing blanks (comment edits keep the hash)."""
+    """C/C++ source without // and /* */ comments, blank lines or indentation (comment edits keep
+    the hash)."""
     out, i, n = [], 0, len(src)
     while i < n:
         if src.startswith("//", i):
@@ -187,7 +188,7 @@ def _strip_comments(src: str) -> str:
         else:
             out.append(src[i])
             i += 1
-    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
+    return "\n".join(line.strip() for line in "".join(out).splitlines() if line.strip())
 
 
 def kernel_sha() -> str:
