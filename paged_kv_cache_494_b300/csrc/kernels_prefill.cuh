@@ -42,10 +42,14 @@ struct PrefillShape {
   static constexpr int kStageBytes = 2 * CB;
   static constexpr int KS = D / 16;
   static constexpr int NT = D / 8;
+  static constexpr int kQBytes = NW * 16 * D * 2;  // each warp's 16 query rows, staged for ldmatrix
 };
 
-__host__ __device__ inline size_t prefill_smem_bytes(int stages, int stage_bytes, int n_seqs, int max_blocks) {
-  return 1024 + static_cast<size_t>(stages) * stage_bytes + static_cast<size_t>(stages) * 16 + 256 +
+// [1 KB alignment slack][ring: stages x stage][query rows][full / empty mbarriers][scan scratch]
+// [query-tile prefix][block-table entries]
+__host__ __device__ inline size_t prefill_smem_bytes(int stages, int stage_bytes, int q_bytes, int n_seqs,
+                                                     int max_blocks) {
+  return 1024 + static_cast<size_t>(stages) * stage_bytes + q_bytes + static_cast<size_t>(stages) * 16 + 256 +
          static_cast<size_t>(n_seqs + 1) * 4 + static_cast<size_t>(max_blocks) * 4;
 }
 
@@ -54,7 +58,7 @@ __device__ __forceinline__ uint32_t prefill_swz(int row, int cb) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(128) paged_prefill_kernel(const __grid_constant__ PrefillArgs a,
+__global__ void __launch_bounds__(128, 4) paged_prefill_kernel(const __grid_constant__ PrefillArgs a,
                                                             const __grid_constant__ TmaMaps maps) {
   using Sh = PrefillShape<D, G>;
   constexpr int NW = Sh::NW, TQW = Sh::TQW, TQ = Sh::TQ, BOX = Sh::BOX, CB = Sh::CB, SB = Sh::kStageBytes;
@@ -67,7 +71,8 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(const __grid_constan
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * SB);
+  unsigned char* qsm = smem + static_cast<size_t>(S) * SB;   // [NW][16 rows][D] bf16, 16-byte blocks swizzled
+  uint64_t* full = reinterpret_cast<uint64_t*>(qsm + Sh::kQBytes);
   uint64_t* empty = full + S;
   int32_t* wsum = reinterpret_cast<int32_t*>(empty + S);
   int32_t* tpref = wsum + 64;          // [n + 1] query-tile prefix over sequences
@@ -206,21 +211,31 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(const __grid_constan
   const int32_t row_ws[2] = {a.window > 0 ? row_pos[0] - a.window + 1 : 0,
                              a.window > 0 ? row_pos[1] - a.window + 1 : 0};
 
-  uint32_t qa[KS][4];
+  // This warp's 16 query rows (row r = token r / G, head r % G; padding rows repeat a real token)
+  // into shared memory: 16-byte block c of row r at ((c & 7) ^ (r & 7)) + (c & ~7), so that the
+  // ldmatrix reads of the A fragments below are free of bank conflicts. Reading q from shared memory
+  // for every chunk instead of holding it in registers keeps the kernel within 128 registers.
+  const uint32_t qw = smem_addr(qsm + static_cast<size_t>(warp) * 16 * D * 2);
   {
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
-    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(qb + ((static_cast<int64_t>(q0) + row_tok[0]) * a.Hq +
-                                                                  h * G + row_head[0]) * D);
-    const uint32_t* r1 = reinterpret_cast<const uint32_t*>(qb + ((static_cast<int64_t>(q0) + row_tok[1]) * a.Hq +
-                                                                  h * G + row_head[1]) * D);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = __ldg(r0 + 8 * ks + t);
-      qa[ks][1] = __ldg(r1 + 8 * ks + t);
-      qa[ks][2] = __ldg(r0 + 8 * ks + 4 + t);
-      qa[ks][3] = __ldg(r1 + 8 * ks + 4 + t);
+    const uint4* qb = static_cast<const uint4*>(a.q);
+    constexpr int NBK = D / 8;   // 16-byte blocks per row
+    unsigned char* qrow_base = qsm + static_cast<size_t>(warp) * 16 * D * 2;
+    for (int idx = lane; idx < 16 * NBK; idx += 32) {
+      const int rr = idx / NBK, c = idx % NBK;
+      const int32_t tk = wt_begin + rr / G;
+      const int32_t tok = warp_has_rows ? min(tk, wt_last) : t_begin;
+      const int hd = rr < TQW * G ? rr % G : 0;
+      const uint4 v = __ldg(qb + ((static_cast<int64_t>(q0) + tok) * a.Hq + h * G + hd) * NBK + c);
+      *reinterpret_cast<uint4*>(qrow_base + rr * D * 2 + ((((c & 7) ^ (rr & 7)) + (c & ~7)) << 4)) = v;
     }
+    __syncwarp();
   }
+  // A fragment of k-step ks: lanes 0..15 address rows 0..15 at dims 16ks.., lanes 16..31 at 16ks+8..
+  const int qrow = lane & 15;
+  auto q_frag = [&](int ks, uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    const int c = 2 * ks + (lane >> 4);
+    ldsm_x4(qw + qrow * D * 2 + ((((c & 7) ^ (qrow & 7)) + (c & ~7)) << 4), a0, a1, a2, a3);
+  };
   float o[NT][4];
 #pragma unroll
   for (int nn = 0; nn < NT; ++nn) o[nn][0] = o[nn][1] = o[nn][2] = o[nn][3] = 0.f;
@@ -246,14 +261,17 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(const __grid_constan
         for (int e = 0; e < 4; ++e) se[nt][e] = so[nt][e] = 0.f;
 #pragma unroll
       for (int p = 0; p < KS / 2; ++p) {
+        uint32_t qe[4], qo[4];
+        q_frag(2 * p, qe[0], qe[1], qe[2], qe[3]);
+        q_frag(2 * p + 1, qo[0], qo[1], qo[2], qo[3]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int tok = 8 * nt + mr;
           const int db = 4 * p + mi;
           uint32_t b0, b1, b2, b3;
           ldsm_x4(kb + (db >> 3) * BOX + prefill_swz(tok, db & 7), b0, b1, b2, b3);
-          mma_bf16_16816(se[nt], qa[2 * p][0], qa[2 * p][1], qa[2 * p][2], qa[2 * p][3], b0, b1);
-          mma_bf16_16816(so[nt], qa[2 * p + 1][0], qa[2 * p + 1][1], qa[2 * p + 1][2], qa[2 * p + 1][3], b2, b3);
+          mma_bf16_16816(se[nt], qe[0], qe[1], qe[2], qe[3], b0, b1);
+          mma_bf16_16816(so[nt], qo[0], qo[1], qo[2], qo[3], b2, b3);
         }
       }
 #pragma unroll

@@ -398,12 +398,13 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   const int g = num_q_heads / d.num_kv_heads;
   using PK = void (*)(pkv_dev::PrefillArgs, pkv_dev::TmaMaps);
   PK kern = nullptr;
-  int tq = 0, stage_bytes = 0;
+  int tq = 0, stage_bytes = 0, q_bytes = 0;
 #define PKV_PREFILL_CASE(DD, GG)                                       \
   if (d.head_dim == DD && g == GG) {                                   \
     kern = pkv_dev::paged_prefill_kernel<DD, GG>;                      \
     tq = pkv_dev::PrefillShape<DD, GG>::TQ;                            \
     stage_bytes = pkv_dev::PrefillShape<DD, GG>::kStageBytes;          \
+    q_bytes = pkv_dev::PrefillShape<DD, GG>::kQBytes;                  \
   }
   PKV_PREFILL_CASE(64, 1) PKV_PREFILL_CASE(64, 2) PKV_PREFILL_CASE(64, 3) PKV_PREFILL_CASE(64, 4)
   PKV_PREFILL_CASE(64, 5) PKV_PREFILL_CASE(64, 6) PKV_PREFILL_CASE(64, 7) PKV_PREFILL_CASE(64, 8)
@@ -412,7 +413,7 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
 #undef PKV_PREFILL_CASE
   if (!kern) return PKV_ERR_INVALID;
   const int stages = env_int("PKV_PREFILL_STAGES", 4);
-  const size_t smem = pkv_dev::prefill_smem_bytes(stages, stage_bytes, n_seqs, d.max_blocks_per_seq);
+  const size_t smem = pkv_dev::prefill_smem_bytes(stages, stage_bytes, q_bytes, n_seqs, d.max_blocks_per_seq);
   if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return PKV_ERR_CUDA;
   const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size;
   if (rows > 0x7fffffffLL) return PKV_ERR_INVALID;
