@@ -629,20 +629,53 @@ def bench_prefill(args):
         "clocks": clocks.summary()}), flush=True)
 
 
+def _profile_pool(pkv, args, fp8: bool):
+    """Pool, block tables and lengths of the workload a --profile-decode run uses (one layer)."""
+    name = {"serve256_fp8": WORKLOAD}.get(args.workload, args.workload)
+    w = synth.workload(name)
+    lens = synth.lengths(w, args.seed)
+    dtype = pkv.FP8 if fp8 else pkv.BF16
+    if w.length_kind == "prefix":
+        # one prompt forked into every child, the prompt released, each child's suffix appended:
+        # the children share the prompt's blocks (the shared-prefix workload)
+        NB = synth.pool_blocks(w, lens)
+        MB = -(-int(lens.max()) // w.block_size) + 1
+        pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs + 1, MB, dtype,
+                        initial_free_list=synth.free_list(NB, args.seed))
+        root = None
+        kids = []
+        for op in synth.prefix_trace(w, args.seed):
+            if op[0] == "new":
+                root = pool.alloc(-1, op[1])[0]
+            elif op[0] == "fork":
+                kids.append(pool.fork(root))
+            elif op[0] == "free":
+                pool.free(root)
+            elif op[2] > 0:
+                pool.alloc(kids[op[1]], op[2])
+        seqs = kids
+    else:
+        pages = sum(-(-int(t) // w.block_size) for t in lens)
+        # the long-context workload's 80 GB pool is cut to twice its pages (same scattered placement
+        # by a seeded permutation) so that the capture holds a few GB
+        NB = synth.pool_blocks(w, lens) if w.pool_rule != "bytes:80e9" else 2 * pages
+        MB = -(-int(lens.max()) // w.block_size) + 1
+        pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs, MB, dtype,
+                        initial_free_list=synth.free_list(NB, args.seed))
+        seqs = [pool.alloc(-1, int(t))[0] for t in lens]
+    tables, l = pool.block_table(seqs)
+    return w, pool, NB, tables, l
+
+
 def profile_decode(args):
-    """Small case for ncu: one layer of the serving workload (about 0.8 GB of bf16 KV, 0.4 GB of fp8,
-    above L2), decode x5. --workload serve256_fp8 profiles the fp8 pool."""
+    """Small case for ncu: one layer of a decode workload, decode x5. serve256_bf16 (default; about
+    0.8 GB of bf16 KV, above L2), serve256_fp8 (the fp8 pool), prefix_cow_bf16 (128 children sharing
+    a 1,024-token prompt: logical bytes above DRAM bytes) or long_split_bf16 (8 x 32,768 tokens,
+    512-token partitions as the workload states)."""
     import torch
     import paged_kv_cache_494_b300 as pkv
     fp8 = args.workload == "serve256_fp8"
-    w = synth.workload(WORKLOAD)
-    lens = synth.lengths(w, args.seed)
-    NB = synth.pool_blocks(w, lens)
-    MB = -(-int(lens.max()) // w.block_size) + 1
-    pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs, MB, pkv.FP8 if fp8 else pkv.BF16,
-                    initial_free_list=synth.free_list(NB, args.seed))
-    seqs = [pool.alloc(-1, int(t))[0] for t in lens]
-    tables, l = pool.block_table(seqs)
+    w, pool, NB, tables, l = _profile_pool(pkv, args, fp8)
     g = torch.Generator(device="cuda").manual_seed(args.seed)
     shape = (NB, w.num_kv_heads, w.block_size, w.head_dim)
     if fp8:
@@ -654,20 +687,23 @@ def profile_decode(args):
     else:
         kc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
         vc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
-    q = torch.randn(w.n_seqs, w.num_q_heads, w.head_dim, device="cuda", dtype=torch.bfloat16, generator=g)
-    out = torch.empty(w.n_seqs, w.num_q_heads, w.head_dim, device="cuda")
-    ws = torch.empty(pool.decode_workspace_bytes(w.n_seqs, w.num_q_heads, 0) // 4 + 4, device="cuda")
+    n = len(l)
+    q = torch.randn(n, w.num_q_heads, w.head_dim, device="cuda", dtype=torch.bfloat16, generator=g)
+    out = torch.empty(n, w.num_q_heads, w.head_dim, device="cuda")
+    pt = w.partition_tokens
+    ws = torch.empty(pool.decode_workspace_bytes(n, w.num_q_heads, pt) // 4 + 4, device="cuda")
     t_tab, t_len = torch.from_numpy(tables).cuda(), torch.from_numpy(l).cuda()
     for _ in range(5):
         if fp8:
-            pool.paged_decode_fp8(out, q, kc, vc, ksc, vsc, t_tab, t_len, w.scale, 0, 0, ws)
+            pool.paged_decode_fp8(out, q, kc, vc, ksc, vsc, t_tab, t_len, w.scale, 0, pt, ws)
         else:
-            pool.paged_decode(out, q, kc, vc, t_tab, t_len, w.scale, 0, ws)
+            pool.paged_decode(out, q, kc, vc, t_tab, t_len, w.scale, pt, ws)
     torch.cuda.synchronize()
     assert pkv.last_error() == pkv.OK
     per = (w.head_dim + 4) * 2 if fp8 else w.head_dim * 2 * 2
     kv = int(l.sum()) * w.num_kv_heads * per
-    print(json.dumps({"profile_decode": args.workload, "layers": 1, "kv_bytes_per_launch": kv, "NB": NB}))
+    print(json.dumps({"profile_decode": args.workload, "layers": 1, "kv_bytes_per_launch": kv, "NB": NB,
+                      "partition_tokens": pt}))
 
 
 def main(argv=None):
@@ -679,7 +715,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=[WORKLOAD, "serve256_fp8", "prefill_bf16"], default=WORKLOAD,
+    ap.add_argument("--workload", choices=[WORKLOAD, "serve256_fp8", "prefill_bf16", "prefix_cow_bf16",
+                                           "long_split_bf16"], default=WORKLOAD,
                     help="serve256_bf16 (the benchmark line), serve256_fp8 (the same step on an fp8 pool) or "
                          "prefill_bf16 (causal prefill kernel line)")
     ap.add_argument("--profile-decode", action="store_true",
@@ -687,6 +724,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.profile_decode:
         return profile_decode(args)
+    if args.workload in ("prefix_cow_bf16", "long_split_bf16"):
+        ap.error(f"--workload {args.workload} is a --profile-decode case (the bench line is serve256_bf16)")
     if args.workload == "prefill_bf16":
         return bench_prefill(args)
     if args.warmup < 3:
