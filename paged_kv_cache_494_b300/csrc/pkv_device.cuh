@@ -78,15 +78,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // 1-D bulk copy (TMA engine) of `bytes` (multiple of 16, both addresses 16-byte aligned) from
-// global memory into this CTA's shared memory; completion is signalled on `bar` as tx bytes.
-__device__ __forceinline__ void bulk_g2s(uint32_t smem_dst, const void* gmem_src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_dst),
-      "l"(gmem_src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Same, with an L2 eviction-priority hint (policy from createpolicy).
+// global memory into this CTA's shared memory, with an L2 eviction-priority hint (policy from
+// createpolicy); completion is signalled on `bar` as tx bytes.
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t smem_dst, const void* gmem_src, uint32_t bytes, uint32_t bar,
                                               uint64_t policy) {
   asm volatile(
@@ -188,13 +181,6 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
       "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
       : "=r"(lo), "=r"(hi)
       : "r"(w));
-}
-
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  const uint16_t c = static_cast<uint16_t>(two_codes & 0xffffu);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
-  return r;
 }
 
 // Two floats -> two FP8 E4M3 codes (round to nearest even, saturated to +-448); `lo` in the low byte.
