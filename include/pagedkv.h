@@ -328,6 +328,16 @@ PKV_API pkv_status pkv_paged_decode_static(const pkv_pool* pool, float* out, con
  * else PKV_OK. pool may be NULL. */
 PKV_API pkv_status pkv_last_error(const pkv_pool* pool);
 
+/* ---- diagnostics -------------------------------------------------------------------------- */
+/* Self-test of the bounded waits of the pipelined kernels (no counterpart on the pages: it checks
+ * this library's failure detection). Enqueues one warp on `stream` that waits, with the same
+ * bounded wait the decode and prefill kernels use, on a shared-memory barrier that nothing
+ * signals. The wait gives up after its poll limit (about a second), records
+ * PKV_ERR_DEVICE_TIMEOUT for pkv_last_error and the kernel returns normally, leaving the CUDA
+ * context usable. gave_up: device int32 (may be NULL), set to 1 when the wait gave up.
+ * Returns PKV_ERR_CUDA if the launch fails. */
+PKV_API pkv_status pkv_selftest_wait_timeout(int32_t* gave_up, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

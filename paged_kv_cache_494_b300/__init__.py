@@ -86,6 +86,7 @@ _SIGS = {
     "pkv_paged_decode_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32,
                                                _vp]),
     "pkv_last_error": (ctypes.c_int, [_vp]),
+    "pkv_selftest_wait_timeout": (ctypes.c_int, [_vp, _vp]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 for _name, (_res, _args) in _SIGS.items():

@@ -21,6 +21,24 @@
 #include "kernels_prefill.cuh"
 #include "pkv_pool.hpp"
 
+namespace pkv_dev {
+
+// One warp waits on a fresh shared-memory mbarrier that nothing arrives on, with the bounded wait of
+// the pipelined kernels: it gives up after kMaxPolls polls, records ERRBIT_TIMEOUT and returns.
+// No copy or other asynchronous operation is in flight, so the block can exit at once.
+__global__ void selftest_wait_kernel(int32_t* gave_up) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool done = mbar_wait_bounded(smem_addr(&bar), 0u);
+  if (threadIdx.x == 0 && gave_up != nullptr) *gave_up = done ? 0 : 1;
+}
+
+}  // namespace pkv_dev
+
 namespace {
 
 using pkv_dev::DecodeArgs;
@@ -614,6 +632,11 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
 }  // namespace
 
 extern "C" {
+
+pkv_status pkv_selftest_wait_timeout(int32_t* gave_up, void* stream) {
+  pkv_dev::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(gave_up);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 pkv_status pkv_last_error(const pkv_pool*) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
