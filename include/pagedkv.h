@@ -16,12 +16,13 @@
  *    solicitudes simultáneas de IA local?", section "PagedAttention divide el estado KV
  *    en bloques de tamaño fijo"; "Paged Attention optimiza el uso de memoria en LLMs",
  *    16-token pages and the page table).
- *  - Finished requests return their unshared blocks to the pool at once (same zimaspace
- *    page, "Los bloques liberados regresan a un conjunto compartido"); the runtime keeps
+ *  - Finished requests return their unshared blocks to the pool at once ("¿Cómo gestiona
+ *    Paged Attention la caché KV...?", "Los bloques liberados regresan a un conjunto
+ *    compartido"); the runtime keeps
  *    block tables and reference counts ("La gestión de bloques tiene sus propios costes").
  *  - Identical prefixes share physical pages; only the page where a request diverges is
- *    copied ("PagedAttention e vLLM", "Approfondimento tecnico"; the elsemanal page's
- *    copy-on-write paragraph). Cancellation releases references without freeing pages
+ *    copied ("PagedAttention e vLLM", "Approfondimento tecnico"; "Paged Attention optimiza
+ *    el uso de memoria en LLMs", copy-on-write paragraph). Cancellation releases references without freeing pages
  *    still in use ("Servicio de modelos de lenguaje con un presupuesto de memoria" §8).
  *  - Decode attention is exact softmax(scale * q.K^T) V, computed blockwise with running
  *    max/sum statistics (same page §6); GQA query heads share a KV head in contiguous
@@ -31,7 +32,8 @@
  *     cache[num_blocks][num_kv_heads][block_size][head_dim]   (dtype of the pool)
  * Token slot s (from pkv_alloc) lives at block s / block_size, offset s % block_size.
  * Block ids are shared by all layers: one block table serves every layer, since every
- * layer stores every token (per-token budget 2*L*Hkv*D*bytes, the auturnal page §3).
+ * layer stores every token (per-token budget 2*L*Hkv*D*bytes, "Servicio de modelos de
+ * lenguaje con un presupuesto de memoria" §3).
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H

@@ -10,7 +10,8 @@ What the pages fix:
   e vLLM", "Approfondimento tecnico"; "Paged Attention optimiza el uso de memoria
   en LLMs", paragraph on 16-token pages and the page table);
 * when a request ends its unshared blocks return to the shared pool at once
-  (same zimaspace page, "Los bloques liberados regresan a un conjunto compartido");
+  ("¿Cómo gestiona Paged Attention la caché KV...?", "Los bloques liberados regresan a
+  un conjunto compartido");
 * the runtime keeps reference counts ("La gestión de bloques tiene sus propios
   costes"); cancellation releases references without freeing pages still in use
   ("Servicio de modelos de lenguaje con un presupuesto de memoria" §8);
