@@ -265,3 +265,148 @@ def test_release_before_frees_only_unshared_blocks():
     # appends continue at the same slots after a release
     st, _, slots, _ = p.alloc(a, 1)
     assert st == am.OK and slots == [p.tables[a][6] * 16 + 100 % 16]
+
+
+# ---- the batched decode-step append (PoolModel.append) ---------------------------------------------
+# A decode step appends one position to each of several sequences at once, all or nothing. What fixes
+# its result is the single-sequence rule above, pinned by the isolation tests: the step must succeed
+# exactly when appending one position to each sequence in turn would, and then leave the same state
+# and report the same slots and copy-on-write pairs; otherwise it must fail and change nothing
+# ("Servicio de modelos de lenguaje con un presupuesto de memoria" §8: shared pages, copied only where
+# a request diverges; "PagedAttention e vLLM", "Approfondimento tecnico").
+
+def _snapshot(p: am.PoolModel):
+    return (list(p.refcount), list(p.free), dict(p.lens), {k: list(v) for k, v in p.tables.items()}, p.n_cow)
+
+
+def sequential_append(p: am.PoolModel, seqs):
+    """One position per sequence through single-sequence appends, on a copy of the model (no fault
+    injection). Returns (status, slots, pairs, copy)."""
+    import copy
+    q = copy.deepcopy(p)
+    q.fail_after = -1
+    slots, pairs = [], []
+    for s in seqs:
+        st, _, sl, pr = q.alloc(s, 1)
+        if st != am.OK:
+            return st, [], [], q
+        slots += sl
+        pairs += pr
+    return am.OK, slots, pairs, q
+
+
+def tight_states(seed, B, n_states, model_cls=am.PoolModel):
+    """Seeded pool states with shared partially filled blocks and almost no free blocks: a few
+    prompts forked several times, some parents freed, the free list then filled down to 0-3 blocks
+    by a filler sequence. Yields (model, sequences to append)."""
+    rng = np.random.default_rng(seed)
+    for _ in range(n_states):
+        NB = int(rng.integers(30, 60))
+        p = model_cls(NB, B, 40, 64, initial_free_list=rng.permutation(NB))
+        roots = []
+        for _ in range(int(rng.integers(1, 4))):
+            st, r, _, _ = p.alloc(-1, int(rng.integers(1, 3 * B)))
+            if st == am.OK:
+                roots.append(r)
+        for r in roots:
+            for _ in range(int(rng.integers(1, 5))):
+                p.fork(r)
+        for r in roots:
+            if rng.random() < 0.5:
+                p.free_seq(r)
+        keep = int(rng.integers(0, 4))
+        if len(p.free) > keep:
+            p.alloc(-1, (len(p.free) - keep) * B)       # filler: takes all but `keep` free blocks
+        live = sorted(p.tables)
+        k = int(rng.integers(1, len(live) + 1))
+        yield p, [int(s) for s in rng.permutation(live)[:k]]
+
+
+def append_pin_failures(model_cls):
+    """Run the append pins against a model class; return the names of those that fail."""
+    failed = []
+    # hand-worked: a parent whose only block is partial (8 of 16), 3 forks, the parent freed -> the
+    # children hold the block 3 times. Appending to all three copies twice (refcount 3 -> 2 -> 1) and
+    # the last holder writes in place, so exactly 2 free blocks suffice; with 1 the step must fail.
+    for nb_free, expect in ((2, am.OK), (1, am.ERR_NO_BLOCKS)):
+        p = model_cls(1 + nb_free, 16, 8, 4)
+        _, par, _, _ = p.alloc(-1, 8)
+        kids = [p.fork(par)[1] for _ in range(3)]
+        p.free_seq(par)
+        before = _snapshot(p)
+        st, slots, pairs = p.append(kids)
+        if st != expect:
+            failed.append(f"tight_{nb_free}")
+            continue
+        if expect == am.OK:
+            blk = before[3][kids[0]][0]
+            if not (len(pairs) == 2 and all(src == blk for src, _ in pairs)
+                    and p.tables[kids[2]] == [blk] and slots[2] == blk * 16 + 8
+                    and p.refcount[blk] == 1 and len(p.free) == 0):
+                failed.append(f"tight_{nb_free}_result")
+        elif _snapshot(p) != before:
+            failed.append("tight_unchanged")
+    # equivalence with single-sequence appends on seeded tight pools
+    for seed in range(3):
+        for B in (1, 4, 16):
+            for p, seqs in tight_states(seed, B, 25, model_cls):
+                before = _snapshot(p)
+                exp_st, exp_slots, exp_pairs, q = sequential_append(p, seqs)
+                try:
+                    st, slots, pairs = p.append(seqs)
+                except AssertionError:
+                    st, slots, pairs = "raised", [], []
+                if exp_st == am.OK:
+                    ok = st == am.OK and list(slots) == exp_slots and list(pairs) == exp_pairs and \
+                        _snapshot(p) == _snapshot(q)
+                else:
+                    ok = st == exp_st and _snapshot(p) == before
+                if not ok:
+                    failed.append("sequential")
+                    break
+            if "sequential" in failed:
+                break
+        if "sequential" in failed:
+            break
+    # duplicate ids are invalid and change nothing
+    p = model_cls(16, 4, 4, 8)
+    _, a, _, _ = p.alloc(-1, 3)
+    before = _snapshot(p)
+    try:
+        st = p.append([a, a])[0]
+    except AssertionError:
+        st = "raised"
+    if st != am.ERR_INVALID or _snapshot(p) != before:
+        failed.append("duplicates")
+    # fault injection counts one decode step as one call, however many sequences it appends to
+    p = model_cls(32, 4, 4, 8, fail_after_n_allocs=4)
+    _, a, _, _ = p.alloc(-1, 3)
+    _, b, _, _ = p.alloc(-1, 5)                     # 2 calls
+    if p.append([a, b])[0] != am.OK:                # the 3rd call
+        failed.append("inject_step")
+    elif p.alloc(a, 1)[0] != am.OK:                 # the 4th call is still allowed
+        failed.append("inject_count")
+    elif p.append([a, b])[0] != am.ERR_NO_BLOCKS:   # the 5th is refused
+        failed.append("inject_refuse")
+    return failed
+
+
+def test_append_pins_hold_for_the_oracle():
+    assert append_pin_failures(am.PoolModel) == []
+
+
+def test_append_hand_worked_tight_pool():
+    """The worked case on its own: 3 holders of one partial block, 2 free blocks -> 2 copies."""
+    p = am.PoolModel(3, 16, 8, 4)
+    _, par, _, _ = p.alloc(-1, 8)
+    kids = [p.fork(par)[1] for _ in range(3)]
+    blk = p.tables[par][0]
+    p.free_seq(par)
+    assert p.refcount[blk] == 3 and len(p.free) == 2
+    st, slots, pairs = p.append(kids)
+    assert st == am.OK
+    assert [src for src, _ in pairs] == [blk, blk]
+    assert sorted(dst for _, dst in pairs) == sorted({0, 1, 2} - {blk})
+    assert p.tables[kids[2]] == [blk] and slots[2] == blk * 16 + 8
+    assert p.stats()["num_cow"] == 2 and p.stats()["num_free"] == 0
+    check_invariants(p)

@@ -129,3 +129,58 @@ def test_c_mutant_is_caught(kind, tmp_path):
     so = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-o", str(so), str(mpath), "-lm"], check=True)
     assert pin_checks(_windowed(native.decode_fn_from(str(so)))) != []
+
+
+# ---- allocator mutants: the batched decode-step append ----------------------------------------------
+
+from oracle import alloc_model as am  # noqa: E402
+from tests.test_oracle_alloc import append_pin_failures  # noqa: E402
+
+
+def _append_mutant(kind):
+    class Mutant(am.PoolModel):
+        def append(self, seqs):
+            seqs = [int(s) for s in seqs]
+            if kind != "no_dup_check" and len(set(seqs)) != len(seqs):
+                return am.ERR_INVALID, [], []
+            if any(s not in self.tables for s in seqs):
+                return am.ERR_NO_SEQ, [], []
+            if any(-(-(self.lens[s] + 1) // self.B) > self.MB for s in seqs):
+                return am.ERR_CAPACITY, [], []
+            if self.fail_after >= 0 and self.n_allocs >= self.fail_after:
+                return am.ERR_NO_BLOCKS, [], []
+            rc = list(self.refcount)
+            need = 0
+            for s in seqs:
+                if self.lens[s] % self.B == 0:
+                    need += 0 if kind == "no_new_block" else 1
+                elif rc[self.tables[s][-1]] > 1:
+                    if kind != "no_replay":
+                        rc[self.tables[s][-1]] -= 1
+                    need += 1
+            if kind != "no_precheck" and need > len(self.free):
+                return am.ERR_NO_BLOCKS, [], []
+            slots, pairs = [], []
+            for s in seqs:
+                st, _, sl, pr = self.alloc(s, 1)
+                if st != am.OK:              # without the precheck a step can stop half-way
+                    return st, slots, pairs
+                if kind != "count_per_seq":
+                    self.n_allocs -= 1
+                slots += sl
+                pairs += pr
+            if kind != "count_per_seq":
+                self.n_allocs += 1
+            return am.OK, slots, pairs
+    return Mutant
+
+
+@pytest.mark.parametrize("kind", ["no_replay", "no_new_block", "no_precheck", "count_per_seq", "no_dup_check"])
+def test_append_mutant_is_caught(kind):
+    assert append_pin_failures(_append_mutant(kind)) != []
+
+
+def test_append_mutant_copy_is_faithful():
+    """The mutant template with no mistake planted passes every pin (so a caught mutant is caught
+    for its planted mistake)."""
+    assert append_pin_failures(_append_mutant("none")) == []
