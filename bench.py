@@ -44,6 +44,9 @@ import synth  # noqa: E402
 WORKLOAD = "serve256_bf16"
 METRIC = "paged-decode KV GB/s read (% of B300 HBM peak); decode seq-steps/sec"
 FALLBACK_HBM_GBS = 6400.0
+NOMINAL_HBM_GBS = 7700.0      # B300 HBM3e datasheet figure (context beside the measured copy peak)
+L2_FLUSH_BYTES = 256 << 20    # a write of this many bytes evicts the 126 MB L2
+PREFILL_KERNEL = "paged_prefill_kernel (mma.sync m16n8k16, P as bf16 hi + lo)"
 
 
 # ------------------------------------------------------------------------------------------------
@@ -144,6 +147,21 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def workload_config(name: str, world: int) -> dict:
+    """The `config` object of a bench line; both arms print the same one for the same workload."""
+    w = synth.workload(WORKLOAD)
+    fp8 = name == "serve256_fp8"
+    return {
+        "workload": name,
+        "description": w.description + (
+            "; fp8 E4M3 pool with per-(token, head) scales (KV bytes = codes + scales)" if fp8 else ""),
+        "n_seqs": w.n_seqs, "layers": w.n_layers, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+        "head_dim": w.head_dim, "block_size": w.block_size,
+        "l2": "inputs larger than L2 (every step reads all KV of 32 layers, >20 GB)",
+        "parallelism": f"replicas x{world}", "partition": "balanced split (partition_tokens=0)",
+    }
 
 
 def measured_peaks():
@@ -250,6 +268,7 @@ class Serve:
         self.out = [torch.empty(self.n, self.Hq, self.D, device=device, dtype=torch.float32) for _ in range(self.L)]
         self.ws = torch.empty(self.pool.decode_workspace_bytes(self.n, self.Hq, 0) // 4 + 4, device=device)
         self.stream = torch.cuda.current_stream(device)
+        self.nvtx = False          # one NVTX range per layer (bench.py --nvtx)
 
     def plan_steps(self, n_steps: int):
         """Host allocator work for n decode steps (slot of each appended token, tables, lengths)."""
@@ -280,7 +299,10 @@ class Serve:
     def run_step(self, step) -> int:
         """Enqueue one step: per layer K1 then decode. Returns the number of kernels launched."""
         slots, tables, lens, _ = step
+        nvtx = self.torch.cuda.nvtx if self.nvtx else None
         for l in range(self.L):
+            if nvtx:
+                nvtx.range_push(f"layer {l}")
             if self.fp8:
                 self.pool.reshape_and_cache_fp8(self.k_new[l], self.v_new[l], slots, self.k_caches[l],
                                                 self.v_caches[l], self.k_scales[l], self.v_scales[l],
@@ -289,6 +311,8 @@ class Serve:
                 self.pool.reshape_and_cache(self.k_new[l], self.v_new[l], slots, self.k_caches[l], self.v_caches[l],
                                             stream=self.stream)
             self.decode(l, tables, lens)
+            if nvtx:
+                nvtx.range_pop()
         return self.L * 2
 
 
@@ -302,6 +326,7 @@ def bench_cuda(args, world, rank, local):
     s = Serve(args.seed + rank, 2 * steps_total + args.warmup + args.steps + 4, device, fp8=fp8)
     pkv = s.pkv
     plan = s.plan_steps(steps_total)
+    s.nvtx = args.nvtx
     Ev = lambda: torch.cuda.Event(enable_timing=True)
 
     for i in range(args.warmup):
@@ -367,18 +392,12 @@ def bench_cuda(args, world, rank, local):
         "dtype": "fp8e4m3" if fp8 else "bf16",
         "accumulate": "f32",
         "data": "synthetic",
-        "config": {
-            "workload": args.workload,
-            "description": synth.workload(WORKLOAD).description + (
-                "; fp8 E4M3 pool with per-(token, head) scales (KV bytes = codes + scales)" if fp8 else ""),
-            "n_seqs": s.n, "layers": s.L, "num_q_heads": s.Hq, "num_kv_heads": s.Hkv, "head_dim": s.D,
-            "block_size": s.B, "mean_context": float(np.mean(plan[args.warmup][3])),
-            "kv_gb_per_step": round(kv_bytes / args.steps / 1e9, 3),
-            "l2": "inputs larger than L2 (every step reads all KV of 32 layers, >20 GB)",
-            "parallelism": f"replicas x{world}", "partition": "balanced split (partition_tokens=0)",
-        },
+        "config": workload_config(args.workload, world),
+        "mean_context": float(np.mean(plan[args.warmup][3])),
+        "kv_gb_per_step": round(kv_bytes / args.steps / 1e9, 3),
         "seq_steps_per_s": round(seq_steps_all / (t_ms_max * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * value / (peak * world), 2),
+        "pct_of_nominal_hbm": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
         "roofline": {
             "bound": "hbm",
             "kernel": "paged_decode_kernel (one pkv_paged_decode call; split units merged in-kernel by log-sum-exp)",
@@ -398,6 +417,10 @@ def bench_cuda(args, world, rank, local):
         line.pop("e2e")
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         line["cpu_baseline"] = cpu_baseline(args, budget_s=args.cpu_seconds)
+    if rank == 0 and world == 1 and not fp8 and not args.no_workloads:
+        del s, plan
+        torch.cuda.empty_cache()
+        line["workloads"] = bench_workloads(args, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -566,7 +589,7 @@ def bench_reference(args, world, rank):
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * t_all / args.steps * w.n_layers, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "description": w.description, "n_seqs": w.n_seqs, "layers": w.n_layers},
+        "config": workload_config(WORKLOAD, world),
         "seq_steps_per_s": round(float(np.median(ss_list)), 3),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -576,10 +599,48 @@ def bench_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def bench_prefill(args):
+class L2Flush:
+    """Writes a buffer larger than L2 on the current stream (between timed launches)."""
+
+    def __init__(self, device):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def time_launches(torch, fn, flush, n_iter: int, stream=None):
+    """Median device time (ms) of fn() over n_iter launches, L2 flushed before each; CUDA events on
+    the launch stream bracket fn() alone."""
+    stream = stream or torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_iter)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return float(np.median([a.elapsed_time(b) for a, b in evs]))
+
+
+def time_back_to_back(torch, fn, n_iter: int, stream=None):
+    """Average device time (ms) of one fn() over n_iter launches enqueued back to back."""
+    stream = stream or torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fn()
+    a.record(stream)
+    for _ in range(n_iter):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n_iter
+
+
+def prefill_entry(args, n_iter: int = 10):
     """Causal paged prefill (prefill_bf16): every position of 16 x 2,048-token prompts is a query.
-    Reports useful attention TFLOP/s (4 * D per (query row, attended key): q.K and p.V) against the
-    measured dense bf16 tensor peak, and KV bytes per launch."""
+    Useful attention TFLOP/s (4 * D per (query row, attended key): q.K and p.V) against the measured
+    dense bf16 tensor peak, L2 flushed before each timed launch."""
     import torch
     import paged_kv_cache_494_b300 as pkv
     w = synth.workload("prefill_bf16")
@@ -599,41 +660,53 @@ def bench_prefill(args):
     out = torch.empty(total, w.num_q_heads, w.head_dim, device="cuda")
     cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).cuda()
     t_tab, t_len = torch.from_numpy(tables).cuda(), torch.from_numpy(l).cuda()
-    for _ in range(args.warmup):
-        pool.paged_prefill(out, q, kc, vc, t_tab, t_len, cu, w.scale)
+    run = lambda: pool.paged_prefill(out, q, kc, vc, t_tab, t_len, cu, w.scale)
+    for _ in range(max(args.warmup, 3)):
+        run()
     torch.cuda.synchronize()
-    Ev = lambda: torch.cuda.Event(enable_timing=True)
-    a, b = Ev(), Ev()
-    with ClockSampler(0) as clocks:
-        a.record()
-        for _ in range(args.steps):
-            pool.paged_prefill(out, q, kc, vc, t_tab, t_len, cu, w.scale)
-        b.record()
-        torch.cuda.synchronize()
+    flush = L2Flush("cuda")
+    t = time_launches(torch, run, flush, n_iter) * 1e-3
     assert pkv.last_error() == pkv.OK
-    t = a.elapsed_time(b) / args.steps * 1e-3
     keys = sum(int(L) * (int(L) + 1) // 2 for L in lens)          # attended (row, key) pairs per head
     flops = 4.0 * w.head_dim * keys * w.num_q_heads
     kv_bytes = int(lens.sum()) * w.num_kv_heads * w.head_dim * 2 * 2
-    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-        peak = float(json.load(f)["bf16_tflops"])
+    peak = measured_tflops()
     tf = flops / t / 1e12
+    return {"workload": "prefill_bf16", "description": w.description, "kernel": PREFILL_KERNEL,
+            "ms_per_launch": round(t * 1e3, 4), "tflops": round(tf, 2), "kv_gb_per_s": round(kv_bytes / t / 1e9, 1),
+            "flops_per_launch": flops,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(tf / peak, 4)},
+            "timing": f"median of {n_iter} launches, L2 flushed before each (CUDA events around the launch)"}
+
+
+def measured_tflops() -> float:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1800.0
+
+
+def bench_prefill(args):
+    """The prefill line on its own (``--workload prefill_bf16``)."""
+    with ClockSampler(0) as clocks:
+        e = prefill_entry(args, n_iter=max(args.steps, 3))
     print(json.dumps({
-        "metric": "paged-prefill causal attention TFLOP/s (useful FLOPs)", "value": round(tf, 2), "unit": "TFLOP/s",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 4),
+        "metric": "paged-prefill causal attention TFLOP/s (useful FLOPs)", "value": e["tflops"], "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": e["ms_per_launch"],
         "higher_is_better": True, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
-        "config": {"workload": "prefill_bf16", "description": w.description},
-        "kv_gb_per_s": round(kv_bytes / t / 1e9, 1),
-        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tf / peak, 4), "note": "mma.sync m16n8k16; P carried as bf16 hi + lo (2 mmas)"},
+        "config": {"workload": "prefill_bf16", "description": e["description"], "l2": "flushed before each launch"},
+        "kv_gb_per_s": e["kv_gb_per_s"], "roofline": e["roofline"], "kernel": e["kernel"],
         "clocks": clocks.summary()}), flush=True)
 
 
-def _profile_pool(pkv, args, fp8: bool):
-    """Pool, block tables and lengths of the workload a --profile-decode run uses (one layer)."""
-    name = {"serve256_fp8": WORKLOAD}.get(args.workload, args.workload)
+def decode_pool(pkv, name: str, seed: int, fp8: bool, full_pool: bool):
+    """Pool, block tables and lengths of one layer of a decode workload, built by the library's
+    allocator as the workload states. full_pool=False cuts the long-context workload's 80 GB pool
+    to twice its pages (same scattered placement) so that an ncu capture holds a few GB."""
     w = synth.workload(name)
-    lens = synth.lengths(w, args.seed)
+    lens = synth.lengths(w, seed)
     dtype = pkv.FP8 if fp8 else pkv.BF16
     if w.length_kind == "prefix":
         # one prompt forked into every child, the prompt released, each child's suffix appended:
@@ -641,10 +714,10 @@ def _profile_pool(pkv, args, fp8: bool):
         NB = synth.pool_blocks(w, lens)
         MB = -(-int(lens.max()) // w.block_size) + 1
         pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs + 1, MB, dtype,
-                        initial_free_list=synth.free_list(NB, args.seed))
+                        initial_free_list=synth.free_list(NB, seed))
         root = None
         kids = []
-        for op in synth.prefix_trace(w, args.seed):
+        for op in synth.prefix_trace(w, seed):
             if op[0] == "new":
                 root = pool.alloc(-1, op[1])[0]
             elif op[0] == "fork":
@@ -658,52 +731,176 @@ def _profile_pool(pkv, args, fp8: bool):
         pages = sum(-(-int(t) // w.block_size) for t in lens)
         # the long-context workload's 80 GB pool is cut to twice its pages (same scattered placement
         # by a seeded permutation) so that the capture holds a few GB
-        NB = synth.pool_blocks(w, lens) if w.pool_rule != "bytes:80e9" else 2 * pages
+        NB = synth.pool_blocks(w, lens) if (full_pool or w.pool_rule != "bytes:80e9") else 2 * pages
         MB = -(-int(lens.max()) // w.block_size) + 1
         pool = pkv.Pool(1, w.num_kv_heads, w.head_dim, w.block_size, NB, w.n_seqs, MB, dtype,
-                        initial_free_list=synth.free_list(NB, args.seed))
+                        initial_free_list=synth.free_list(NB, seed))
         seqs = [pool.alloc(-1, int(t))[0] for t in lens]
     tables, l = pool.block_table(seqs)
     return w, pool, NB, tables, l
 
 
+class DecodeProblem:
+    """One layer of a decode workload on the device: pool, caches, q, tables, output, workspace."""
+
+    def __init__(self, name: str, seed: int, fp8: bool = False, full_pool: bool = True,
+                 partition_tokens=None):
+        import torch
+        import paged_kv_cache_494_b300 as pkv
+        self.torch, self.pkv, self.fp8 = torch, pkv, fp8
+        w, pool, NB, tables, l = decode_pool(pkv, name, seed, fp8, full_pool)
+        self.w, self.pool, self.NB = w, pool, NB
+        g = torch.Generator(device="cuda").manual_seed(seed)
+        if fp8:
+            ks_, vs_, ss_ = pool.fp8_shapes()
+            self.kc = torch.randint(0, 0x7E, ks_, device="cuda", dtype=torch.uint8, generator=g)
+            self.vc = torch.randint(0, 0x7E, vs_, device="cuda", dtype=torch.uint8, generator=g)
+            self.ksc = torch.rand(ss_, device="cuda", generator=g) * 0.01
+            self.vsc = torch.rand(ss_, device="cuda", generator=g) * 0.01
+        else:
+            dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+            shape = (NB, w.num_kv_heads, w.block_size, w.head_dim)
+            self.kc = torch.randn(shape, device="cuda", dtype=dt, generator=g)
+            self.vc = torch.randn(shape, device="cuda", dtype=dt, generator=g)
+        self.n = len(l)
+        qdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.q = torch.randn(self.n, w.num_q_heads, w.head_dim, device="cuda", dtype=qdt, generator=g)
+        self.out = torch.empty(self.n, w.num_q_heads, w.head_dim, device="cuda")
+        self.pt = w.partition_tokens if partition_tokens is None else partition_tokens
+        self.ws = torch.empty(pool.decode_workspace_bytes(self.n, w.num_q_heads, self.pt) // 4 + 4, device="cuda")
+        self.tab, self.lens = torch.from_numpy(tables).cuda(), torch.from_numpy(l).cuda()
+        self.lens_host = l
+        per = (w.head_dim + 4) * 2 if fp8 else w.head_dim * 2 * w.elem_bytes
+        self.kv_bytes = int(l.sum()) * w.num_kv_heads * per      # logical KV bytes one launch reads
+
+    def run(self):
+        if self.fp8:
+            self.pool.paged_decode_fp8(self.out, self.q, self.kc, self.vc, self.ksc, self.vsc, self.tab, self.lens,
+                                       self.w.scale, 0, self.pt, self.ws)
+        else:
+            self.pool.paged_decode(self.out, self.q, self.kc, self.vc, self.tab, self.lens, self.w.scale, self.pt,
+                                   self.ws)
+
+
+def decode_entry(name: str, seed: int, peak: float, flush, partition_tokens=None, n_iter: int = 20):
+    """One decode workload: median of n_iter launches with L2 flushed before each (the number
+    reported for every workload), and the average of n_iter launches back to back. GB/s and the
+    roofline fraction use the logical KV bytes a launch reads; where the committed ncu record of the
+    same kernel code has the launch's DRAM bytes, they are reported too (and the fraction on DRAM
+    bytes for the shared-prefix workload, whose shared pages are served from L2)."""
+    import torch
+    p = DecodeProblem(name, seed, partition_tokens=partition_tokens)
+    for _ in range(3):
+        p.run()
+    torch.cuda.synchronize()
+    assert p.pkv.last_error() == p.pkv.OK
+    t = time_launches(torch, p.run, flush, n_iter)
+    tb = time_back_to_back(torch, p.run, n_iter)
+    assert p.pkv.last_error() == p.pkv.OK
+    gbs = p.kv_bytes / (t * 1e-3) / 1e9
+    e = {"workload": name, "partition_tokens": p.pt, "n_seqs": p.n, "num_q_heads": p.w.num_q_heads,
+         "num_kv_heads": p.w.num_kv_heads, "block_size": p.w.block_size, "pool_blocks": p.NB,
+         "mean_context": round(float(np.mean(p.lens_host)), 1), "kv_bytes_per_launch": p.kv_bytes,
+         "us_per_launch": round(1e3 * t, 2), "gb_per_s": round(gbs, 1),
+         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                      "frac": round(gbs / peak, 4)},
+         "b2b_us_per_launch": round(1e3 * tb, 2), "b2b_gb_per_s": round(p.kv_bytes / (tb * 1e-3) / 1e9, 1),
+         "timing": f"median of {n_iter} launches, L2 flushed before each; b2b = mean of {n_iter} launches "
+                   "back to back (no flush)"}
+    key = name if (partition_tokens is None or partition_tokens == p.w.partition_tokens) else None
+    rec = decode_traffic_record(key) if key else None
+    if rec is not None:
+        dram = int(rec["bytes_per_launch_profile"] * p.kv_bytes / rec["algorithmic_bytes_profile"])
+        e["dram_bytes_per_launch"] = dram
+        if p.w.length_kind == "prefix":
+            e["roofline"]["achieved_logical"] = e["roofline"]["achieved"]
+            e["roofline"]["achieved"] = round(dram / (t * 1e-3) / 1e9, 1)
+            e["roofline"]["frac"] = round(dram / (t * 1e-3) / 1e9 / peak, 4)
+            e["roofline"]["basis"] = "ncu DRAM bytes per launch (shared prompt pages are read from L2)"
+    elif p.w.length_kind == "prefix":
+        e["roofline"]["basis"] = "logical bytes (no ncu DRAM record for this kernel code)"
+    del p
+    torch.cuda.empty_cache()
+    return e
+
+
+def fp8_step_entry(args, peak: float, local: int):
+    """The serving step on an fp8 pool, timed like the headline value (K steps back to back on the
+    launch stream, > 10 GB of codes per step), and its decode launches back to back (roofline)."""
+    import torch
+    device = torch.device("cuda", local)
+    n_steps = 2 * args.steps + args.warmup
+    s = Serve(args.seed, 2 * n_steps + 4, device, fp8=True)
+    plan = s.plan_steps(n_steps)
+    for i in range(args.warmup):
+        s.run_step(plan[i])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s.stream)
+    for k in range(args.steps):
+        s.run_step(plan[args.warmup + k])
+    b.record(s.stream)
+    torch.cuda.synchronize()
+    t_step = a.elapsed_time(b) / args.steps
+    kv = sum(s.kv_bytes(plan[args.warmup + k][3]) for k in range(args.steps)) / args.steps
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(s.stream)
+    for k in range(args.steps):
+        _, tab, ln, _ = plan[args.warmup + args.steps + k]
+        for l in range(s.L):
+            s.decode(l, tab, ln)
+    r1.record(s.stream)
+    torch.cuda.synchronize()
+    assert s.pkv.last_error() == s.pkv.OK
+    dec_ms = r0.elapsed_time(r1) / (args.steps * s.L)
+    dec_bytes = sum(s.kv_bytes(plan[args.warmup + args.steps + k][3]) for k in range(args.steps)) / (args.steps * s.L)
+    ach = dec_bytes / (dec_ms * 1e-3) / 1e9
+    e = {"workload": "serve256_fp8", "ms_per_step": round(t_step, 4), "kv_gb_per_step": round(kv / 1e9, 3),
+         "gb_per_s": round(kv / (t_step * 1e-3) / 1e9, 1),
+         "seq_steps_per_s": round(s.n / (t_step * 1e-3), 1),
+         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                      "frac": round(ach / peak, 4), "mean_launch_us": round(1e3 * dec_ms, 2),
+                      "kernel": "paged_decode_kernel<Fp8Math<4>,128,4>"},
+         "timing": f"{args.steps} steps back to back (32 layers of cache write + decode each), inputs larger "
+                   "than L2; roofline = decode launches of the next steps back to back"}
+    del s
+    torch.cuda.empty_cache()
+    return e
+
+
+def bench_workloads(args, local: int):
+    """Every workload of the benchmark set, one entry each (see decode_entry / fp8_step_entry /
+    prefill_entry), with the clocks seen while they ran."""
+    import torch
+    peak, _ = measured_peaks()
+    flush = L2Flush(torch.device("cuda", local))
+    out = {}
+    with ClockSampler(local) as clocks:
+        out["tiny_f32"] = decode_entry("tiny_f32", args.seed, peak, flush)
+        out["gqa5_bf16"] = decode_entry("gqa5_bf16", args.seed, peak, flush)
+        out["prefix_cow_bf16"] = decode_entry("prefix_cow_bf16", args.seed, peak, flush)
+        out["long_split_bf16"] = decode_entry("long_split_bf16", args.seed, peak, flush)
+        out["long_split_bf16_balanced"] = decode_entry("long_split_bf16", args.seed, peak, flush, partition_tokens=0)
+        out["serve256_fp8"] = fp8_step_entry(args, peak, local)
+        out["prefill_bf16"] = prefill_entry(args)
+    out["clocks"] = clocks.summary()
+    return out
+
+
 def profile_decode(args):
     """Small case for ncu: one layer of a decode workload, decode x5. serve256_bf16 (default; about
-    0.8 GB of bf16 KV, above L2), serve256_fp8 (the fp8 pool), prefix_cow_bf16 (128 children sharing
-    a 1,024-token prompt: logical bytes above DRAM bytes) or long_split_bf16 (8 x 32,768 tokens,
-    512-token partitions as the workload states)."""
-    import torch
-    import paged_kv_cache_494_b300 as pkv
+    0.8 GB of bf16 KV, above L2), serve256_fp8 (the fp8 pool), gqa5_bf16, tiny_f32, prefix_cow_bf16
+    (128 children sharing a 1,024-token prompt: logical bytes above DRAM bytes) or long_split_bf16
+    (8 x 32,768 tokens, 512-token partitions as the workload states; pool cut to twice its pages)."""
     fp8 = args.workload == "serve256_fp8"
-    w, pool, NB, tables, l = _profile_pool(pkv, args, fp8)
-    g = torch.Generator(device="cuda").manual_seed(args.seed)
-    shape = (NB, w.num_kv_heads, w.block_size, w.head_dim)
-    if fp8:
-        ks_, vs_, ss_ = pool.fp8_shapes()
-        kc = torch.randint(0, 0x7E, ks_, device="cuda", dtype=torch.uint8, generator=g)
-        vc = torch.randint(0, 0x7E, vs_, device="cuda", dtype=torch.uint8, generator=g)
-        ksc = torch.rand(ss_, device="cuda", generator=g) * 0.01
-        vsc = torch.rand(ss_, device="cuda", generator=g) * 0.01
-    else:
-        kc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
-        vc = torch.randn(shape, device="cuda", dtype=torch.bfloat16, generator=g)
-    n = len(l)
-    q = torch.randn(n, w.num_q_heads, w.head_dim, device="cuda", dtype=torch.bfloat16, generator=g)
-    out = torch.empty(n, w.num_q_heads, w.head_dim, device="cuda")
-    pt = w.partition_tokens
-    ws = torch.empty(pool.decode_workspace_bytes(n, w.num_q_heads, pt) // 4 + 4, device="cuda")
-    t_tab, t_len = torch.from_numpy(tables).cuda(), torch.from_numpy(l).cuda()
+    name = WORKLOAD if fp8 else args.workload
+    p = DecodeProblem(name, args.seed, fp8=fp8, full_pool=False)
     for _ in range(5):
-        if fp8:
-            pool.paged_decode_fp8(out, q, kc, vc, ksc, vsc, t_tab, t_len, w.scale, 0, pt, ws)
-        else:
-            pool.paged_decode(out, q, kc, vc, t_tab, t_len, w.scale, pt, ws)
-    torch.cuda.synchronize()
-    assert pkv.last_error() == pkv.OK
-    per = (w.head_dim + 4) * 2 if fp8 else w.head_dim * 2 * 2
-    kv = int(l.sum()) * w.num_kv_heads * per
-    print(json.dumps({"profile_decode": args.workload, "layers": 1, "kv_bytes_per_launch": kv, "NB": NB,
-                      "partition_tokens": pt}))
+        p.run()
+    p.torch.cuda.synchronize()
+    assert p.pkv.last_error() == p.pkv.OK
+    print(json.dumps({"profile_decode": args.workload, "layers": 1, "kv_bytes_per_launch": p.kv_bytes, "NB": p.NB,
+                      "partition_tokens": p.pt}))
 
 
 def main(argv=None):
@@ -715,8 +912,11 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload entries (every other benchmark configuration) of the line")
+    ap.add_argument("--nvtx", action="store_true", help="one NVTX range per layer in the timed steps")
     ap.add_argument("--workload", choices=[WORKLOAD, "serve256_fp8", "prefill_bf16", "prefix_cow_bf16",
-                                           "long_split_bf16"], default=WORKLOAD,
+                                           "long_split_bf16", "gqa5_bf16", "tiny_f32"], default=WORKLOAD,
                     help="serve256_bf16 (the benchmark line), serve256_fp8 (the same step on an fp8 pool) or "
                          "prefill_bf16 (causal prefill kernel line)")
     ap.add_argument("--profile-decode", action="store_true",
@@ -724,7 +924,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.profile_decode:
         return profile_decode(args)
-    if args.workload in ("prefix_cow_bf16", "long_split_bf16"):
+    if args.workload in ("prefix_cow_bf16", "long_split_bf16", "gqa5_bf16", "tiny_f32"):
         ap.error(f"--workload {args.workload} is a --profile-decode case (the bench line is serve256_bf16)")
     if args.workload == "prefill_bf16":
         return bench_prefill(args)

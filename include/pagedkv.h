@@ -236,7 +236,12 @@ PKV_API pkv_status pkv_copy_blocks(const pkv_pool* pool, void* const* k_caches, 
  * tokens, each computed separately and merged the same way. The result never depends on where
  * blocks are placed physically (it may depend, to rounding, on a sequence's batch position).
  * workspace: device scratch of at least pkv_decode_workspace_bytes(...) bytes (may be NULL if that
- * is 0); its contents need no initialisation. Concurrent calls must not share a workspace. */
+ * is 0); its contents need no initialisation. Concurrent calls must not share a workspace.
+ * Batch size: n_seqs <= 16384. Every CTA also keeps 4 bytes per sequence of prefix sums in shared
+ * memory beside its copy ring (8 with partition_tokens > 0 or a window, 12 with both); a batch whose
+ * arrays do not fit the device's per-block shared memory is rejected with PKV_ERR_INVALID (on B300
+ * with bf16 D = 128 that happens only with both partitions and a window, above 13,796 sequences).
+ * Large batches lower the number of resident CTAs per SM. */
 PKV_API pkv_status pkv_paged_decode(const pkv_pool* pool, float* out, const void* q, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                             int32_t n_seqs, int32_t num_q_heads, float scale, int32_t partition_tokens,
@@ -313,7 +318,10 @@ PKV_API size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t n_seqs, 
  * until the process exits. It calls no allocator (no cudaMalloc, no cudaFree, no library routine
  * that allocates).
  *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress with
- *    that device current) and remembers it; make that first call before any stream capture.
+ *    that device current) and remembers it with the id of the device's context; make that first
+ *    call before any stream capture. A call that finds another context current (the device was
+ *    reset, e.g. by cudaDeviceReset, and its context re-created) looks the address up again, since
+ *    the array then lives at a new address; that call, too, should come before any capture.
  *  - Every call on a device uses the same array. Its contents need no initialisation (each call
  *    writes every scratch entry it later reads), but calls whose kernels overlap on the GPU (other
  *    streams, other threads) race on it: serialise them, e.g. on one stream.

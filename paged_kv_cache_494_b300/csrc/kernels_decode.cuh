@@ -251,19 +251,21 @@ __device__ __forceinline__ int64_t item_start(const int32_t* pref, const int32_t
 }
 
 // Shared-memory carve-up of the decode kernel: [1 KB alignment slack][ring: per warp `stages` stages]
-// [mbarriers][64-int scan scratch][pref][ipref][cfirst]. Stages start on 1024-byte boundaries
-// (128-byte swizzle atoms).
+// [mbarriers][64-int scan scratch][pref][ipref (fixed partitions only)][cfirst (window only)].
+// Stages start on 1024-byte boundaries (128-byte swizzle atoms).
 __host__ __device__ inline size_t decode_ring_bytes(int nw, int stages, int stage_bytes) {
   return static_cast<size_t>(nw) * stages * stage_bytes;
 }
-__host__ __device__ inline size_t decode_smem_bytes(int nw, int stages, int stage_bytes, int n_seqs) {
+__host__ __device__ inline size_t decode_smem_bytes(int nw, int stages, int stage_bytes, int n_seqs, bool parts,
+                                                    bool window) {
   return 1024 + decode_ring_bytes(nw, stages, stage_bytes) + static_cast<size_t>(nw) * stages * 8 + 256 +
-         3 * static_cast<size_t>(n_seqs + 1) * 4;
+         (1 + (parts ? 1 : 0) + (window ? 1 : 0)) * static_cast<size_t>(n_seqs + 1) * 4;
 }
 
 // Block-wide exclusive prefix sums over sequences of chunk counts (pref) and partition counts
-// (ipref); pref[n] / ipref[n] hold the totals; cfirst[b] is the first chunk of sequence b that
-// the attention reads (0, or the chunk holding position len - window). Every thread of the CTA
+// (ipref, fixed-partition mode only, else null); pref[n] / ipref[n] hold the totals; cfirst[b]
+// (window only, else null) is the first chunk of sequence b that the attention reads (0, or the
+// chunk holding position len - window). Every thread of the CTA
 // takes part. Lengths are loaded kPrefixBatch tiles at a time so that their latencies overlap.
 // wsum: 64 ints of smem.
 constexpr int kPrefixBatch = 8;
@@ -321,8 +323,8 @@ __device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref,
       const int32_t b = base + k * nt + tid;
       if (b < n) {
         pref[b] = carry_c + pc + ic - c;
-        ipref[b] = carry_i + pi + ii - ci;
-        cfirst[b] = c0;
+        if (ipref) ipref[b] = carry_i + pi + ii - ci;
+        if (cfirst) cfirst[b] = c0;
       }
       carry_c += tc;
       carry_i += ti;
@@ -331,7 +333,7 @@ __device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref,
   }
   if (tid == 0) {
     pref[n] = carry_c;
-    ipref[n] = carry_i;
+    if (ipref) ipref[n] = carry_i;
   }
 }
 
@@ -966,8 +968,8 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + decode_ring_bytes(NW, S, SB)) + warp * S;
   int32_t* wsum = reinterpret_cast<int32_t*>(smem + decode_ring_bytes(NW, S, SB) + static_cast<size_t>(NW) * S * 8);
   int32_t* pref = wsum + 64;
-  int32_t* ipref = pref + (n + 1);
-  int32_t* cfirst = ipref + (n + 1);
+  int32_t* ipref = PC > 0 ? pref + (n + 1) : nullptr;
+  int32_t* cfirst = a.window > 0 ? pref + (PC > 0 ? 2 : 1) * (n + 1) : nullptr;
 
   // Arrival counters of split units whose segments all belong to this CTA, indexed by the unit's
   // first warp within the CTA (a warp is the first warp of at most one split unit). wsum[16..24) is
@@ -1020,7 +1022,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   Cursor pf = locate(pref, n, Hkv, lo);
   int32_t p_pg = 0, p_sub = 0;
   auto p_unit_start = [&]() {
-    const int32_t ch = cfirst[pf.b] + pf.c;
+    const int32_t ch = (cfirst ? cfirst[pf.b] : 0) + pf.c;
     p_pg = ch / cpb;
     p_sub = ch - p_pg * cpb;
     // warm L2 with the unit's queries: load_q reads them when the consumer gets here
@@ -1120,7 +1122,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
       aborted = true;
       break;
     }
-    const int32_t tok_abs = (cfirst[cc.b] + cc.c) * kChunk;
+    const int32_t tok_abs = ((cfirst ? cfirst[cc.b] : 0) + cc.c) * kChunk;
     const int32_t vhi = min(kChunk, len_b - tok_abs);
     const int32_t vlo = a.window > 0 ? max(0, len_b - a.window - tok_abs) : 0;
     if (!Math::kMaskVariants || vlo > 0 || vhi < kChunk)
@@ -1237,8 +1239,9 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     }
   }
   if (aborted) {
-    // Drain the copies this warp still has in flight (bounded), then leave.
-    for (int64_t k = i + 1; k < issued; ++k)
+    // Drain the copies this warp still has in flight, the one whose wait gave up included (it may
+    // only have been slow), each with one more bounded wait, then leave.
+    for (int64_t k = i; k < issued; ++k)
       mbar_wait_bounded(smem_addr(bars + static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1));
   }
   if (pub) publish();

@@ -299,7 +299,20 @@ unsigned long long next_call_tag() {
   return ((counter.fetch_add(1, std::memory_order_relaxed) << 1) | 1ull) & 0xffffffffffffull;
 }
 
-pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t partition_tokens, DecodePlan* out) {
+// Largest dynamic shared memory one block may opt into on the current device (cached per device).
+size_t max_smem_optin() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v > 0) return static_cast<size_t>(v);
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  cached[dev].store(v, std::memory_order_relaxed);
+  return static_cast<size_t>(v);
+}
+
+pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t partition_tokens, int32_t window,
+                       DecodePlan* out) {
   const pkv_pool_desc& d = p->desc;
   if (n_seqs < 0 || Hq <= 0 || Hq % d.num_kv_heads != 0) return PKV_ERR_INVALID;
   if (d.block_size % pkv_dev::kChunk != 0) return PKV_ERR_INVALID;
@@ -311,7 +324,11 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   if (!pl.k.decode) return PKV_ERR_INVALID;
   pl.nw = env_int("PKV_DECODE_WARPS", 4);
   pl.stages = env_int("PKV_DECODE_STAGES", 2);
-  pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.stage_bytes, n_seqs);
+  pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.stage_bytes, n_seqs, partition_tokens > 0, window > 0);
+  // every CTA keeps per-sequence prefix sums in shared memory: the batch must fit beside the ring
+  const size_t smem_max = max_smem_optin();
+  if (smem_max == 0) return PKV_ERR_CUDA;
+  if (pl.smem > smem_max) return PKV_ERR_INVALID;
   if (!ensure_smem(reinterpret_cast<const void*>(pl.k.decode), pl.smem)) return PKV_ERR_CUDA;
   const int per_sm = occupancy(reinterpret_cast<const void*>(pl.k.decode), pl.nw * 32, pl.smem);
   const int sms = num_sms();
@@ -465,7 +482,7 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
 size_t pkv_decode_workspace_bytes(const pkv_pool* p, int32_t n_seqs, int32_t num_q_heads, int32_t partition_tokens) {
   if (!p) return 0;
   DecodePlan pl;
-  if (plan_decode(p, n_seqs, num_q_heads, partition_tokens, &pl) != PKV_OK) return 0;
+  if (plan_decode(p, n_seqs, num_q_heads, partition_tokens, 0, &pl) != PKV_OK) return 0;
   return pl.ws_bytes;
 }
 
@@ -574,7 +591,7 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
     return PKV_ERR_INVALID;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID;
   DecodePlan pl;
-  const pkv_status st = plan_decode(p, n_seqs, num_q_heads, partition_tokens, &pl);
+  const pkv_status st = plan_decode(p, n_seqs, num_q_heads, partition_tokens, window, &pl);
   if (st != PKV_OK) return st;
   if (workspace_bytes < pl.ws_bytes || (pl.ws_bytes > 0 && (!workspace || !aligned16(workspace))))
     return PKV_ERR_INVALID;
@@ -655,26 +672,63 @@ pkv_status pkv_last_error(const pkv_pool*) {
 // pkv_paged_decode_static: the same decode with scratch compiled into the library, for callers
 // that may not allocate device memory. The array below is part of the module image: each device
 // that loads the library holds it until the process exits. Host code must not use its name as an
-// address (on the host it is only a stand-in); the device address is looked up once per device.
+// address (on the host it is only a stand-in); the device address is looked up once per device
+// and context (again after the device's context was reset and re-created).
 // ---------------------------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
 
 namespace {
 
 std::mutex g_static_mu;
-void* g_static_ptr[64] = {};
+struct StaticScratch {
+  unsigned long long ctx_id = 0;  // context the address belongs to (0: not looked up yet)
+  void* ptr = nullptr;
+};
+StaticScratch g_static[64];
 
-// Device address of g_static_scratch on the current device (looked up on first use per device).
+// Unique id of the calling thread's current CUDA context (cuCtxGetId: ids are never reused within
+// a process, unlike context handles), or 0 if it cannot be read.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_static_scratch on the current device. It is looked up with the device
+// current the first time the device is used, and again whenever the device's context is not the
+// one the address was taken in (the primary context was reset and re-created), since the module
+// and its array are then loaded anew.
 pkv_status static_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  unsigned long long ctx = current_context_id();   // 0 when no context is current on this thread yet
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (g_static_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
+  if (g_static[dev].ptr == nullptr || ctx == 0 || g_static[dev].ctx_id != ctx) {
+    void* ptr = nullptr;   // the lookup also makes the device's primary context current
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) return PKV_ERR_CUDA;
-    g_static_ptr[dev] = ptr;
+    ctx = current_context_id();
+    if (ctx == 0) return PKV_ERR_CUDA;
+    g_static[dev].ptr = ptr;
+    g_static[dev].ctx_id = ctx;
   }
-  *out = g_static_ptr[dev];
+  *out = g_static[dev].ptr;
   return PKV_OK;
 }
 

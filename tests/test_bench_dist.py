@@ -54,3 +54,7 @@ def test_reference_arm_prints_once_under_torchrun():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+    # the reference arm names the same workload with the same config object as the CUDA arm
+    sys.path.insert(0, ROOT)
+    import bench
+    assert rec["config"] == bench.workload_config(bench.WORKLOAD, 2)

@@ -271,3 +271,18 @@ def test_prefix_cache_requests_decode(path):
     err = float(np.max(np.abs(out.double().cpu().numpy() - ref)))
     assert err <= 2e-3, err
     assert pkv.last_error() == pkv.OK
+
+
+def test_largest_batch_and_the_shared_memory_limit():
+    """16,384 sequences (the largest batch the entry point takes) decode correctly; where the
+    per-sequence prefix arrays of a call (12 bytes per sequence with partitions and a window) no
+    longer fit beside a CTA's copy ring, the call is refused before anything is enqueued."""
+    rng = np.random.default_rng(91)
+    c = Case(lengths=rng.integers(1, 41, size=16384).tolist(), Hq=8, Hkv=1, D=128, B=16, dtype="bf16", seed=91)
+    check(c, c.gpu_decode(0), c.oracle_decode())
+    check(c, c.gpu_decode(64), c.oracle_decode())
+    check(c, c.gpu_decode(0, window=24), c.oracle_decode(window=24))
+    with pytest.raises(pkv.PagedKVError) as e:
+        c.gpu_decode(64, window=24)
+    assert e.value.status == pkv.ERR_INVALID
+    assert pkv.last_error() == pkv.OK
