@@ -241,7 +241,11 @@ PKV_API pkv_status pkv_copy_blocks(const pkv_pool* pool, void* const* k_caches, 
  * memory beside its copy ring (8 with partition_tokens > 0 or a window, 12 with both); a batch whose
  * arrays do not fit the device's per-block shared memory is rejected with PKV_ERR_INVALID (on B300
  * with bf16 D = 128 that happens only with both partitions and a window, above 13,796 sequences).
- * Large batches lower the number of resident CTAs per SM. */
+ * Large batches lower the number of resident CTAs per SM.
+ * CUDA graphs: a call may be captured in a graph and the graph replayed any number of times (the
+ * device pointers and sizes of the call are baked into the graph); every replay computes what a
+ * direct call would. Make one direct call of the same shape before capturing: the first call of a
+ * shape sets the kernel's shared-memory limit and looks up its occupancy. */
 PKV_API pkv_status pkv_paged_decode(const pkv_pool* pool, float* out, const void* q, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                             int32_t n_seqs, int32_t num_q_heads, float scale, int32_t partition_tokens,

@@ -27,7 +27,9 @@
 //    one CTA count arrivals in shared memory under CTA-scope fences; the others use global
 //    counters under GPU-scope fences. Global counters carry a tag unique to the call in their high
 //    48 bits, so they never need clearing: a count left by an earlier call (or never written)
-//    carries another tag and restarts at 1.
+//    carries another tag and restarts at 1. The warp that merges a unit (all its parts have
+//    arrived, nothing else touches the counter in this launch) also sets the counter back to 0, so
+//    a launch replayed with the same tag (a captured CUDA graph) starts from zero too.
 //  * The split depends only on the context lengths, never on physical block ids, so results are
 //    bitwise invariant under any placement of the blocks.
 #pragma once
@@ -1107,6 +1109,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
       fence_acq_rel_gpu();
       __syncwarp();
       merge_unit<D, G, false, false>(a, pub_b, pub_h, pub_parts, pub_wf, pub_kind, lane);
+      if (lane == 0) a.ws_count[static_cast<int64_t>(pub_b) * Hkv + pub_h] = 0ull;   // every part has arrived
     }
     pub = false;
   };
@@ -1247,10 +1250,12 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   if (pub) publish();
   pdl_launch_dependents();
   if (pend) {
-    if (pend_cta)
+    if (pend_cta) {
       merge_unit<D, G, true, true>(a, pend_b, pend_h, pend_parts, pend_wf, pend_kind, lane);
-    else
+    } else {
       merge_unit<D, G, true, false>(a, pend_b, pend_h, pend_parts, pend_wf, pend_kind, lane);
+      if (lane == 0) a.ws_count[static_cast<int64_t>(pend_b) * Hkv + pend_h] = 0ull;   // every part has arrived
+    }
   }
 }
 

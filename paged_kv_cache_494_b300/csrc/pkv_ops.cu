@@ -19,6 +19,7 @@
 #include "kernels_cache.cuh"
 #include "kernels_decode.cuh"
 #include "kernels_prefill.cuh"
+#include "kernels_prefill_tc.cuh"
 #include "pkv_pool.hpp"
 
 namespace pkv_dev {
@@ -146,6 +147,14 @@ KernelPair pick_g(int dtype, int g, bool simt) {
   }
 }
 
+// Prefill runs on the tcgen05 kernel unless PKV_PREFILL_PATH=mma (the mma.sync kernel, kept to
+// cross-check the two) or the batch has more sequences than the tcgen05 kernel keeps in shared memory.
+constexpr int32_t kPrefillTcMaxSeqs = 2048;
+bool prefill_path_tc() {
+  const char* s = std::getenv("PKV_PREFILL_PATH");
+  return !(s && std::strcmp(s, "mma") == 0);
+}
+
 // PKV_DECODE_PATH=simt selects the CUDA-core path for bf16 as well (used to cross-check paths).
 bool force_simt() {
   const char* s = std::getenv("PKV_DECODE_PATH");
@@ -226,6 +235,20 @@ bool encode_fp8_maps(pkv_dev::TmaMaps* maps, const void* k_cache, const void* v_
   cuuint32_t vbox[2] = {static_cast<cuuint32_t>(pkv_dev::kChunk), static_cast<cuuint32_t>(d.head_dim)};
   return fn(&maps->v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(v_cache), vdims, vstr, vbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q of a prefill call as a 3-D bf16 array [total_q][Hq][D], boxes of (128 / G) tokens x G heads x 64
+// dims with 128-byte swizzle: one box lands as the rows (token, head of the group) of a Q tile.
+bool encode_q_map(CUtensorMap* m, const void* q, int32_t total_q, int32_t Hq, int32_t D, int32_t G) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(total_q)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hq) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(pkv_dev::kTcRows / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -431,6 +454,56 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   if (num_q_heads <= 0 || num_q_heads % d.num_kv_heads != 0) return PKV_ERR_INVALID;
   if (n_seqs > 16384 || d.max_blocks_per_seq > 8192) return PKV_ERR_INVALID;
   const int g = num_q_heads / d.num_kv_heads;
+  const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size;
+  if (rows > 0x7fffffffLL || d.num_kv_heads > 65535) return PKV_ERR_INVALID;
+  pkv_dev::PrefillArgs a;
+  a.out = out;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.cu_q = cu_q;
+  a.n_seqs = n_seqs;
+  a.Hq = num_q_heads;
+  a.Hkv = d.num_kv_heads;
+  a.B = d.block_size;
+  a.NB = d.num_blocks;
+  a.MB = d.max_blocks_per_seq;
+  a.window = window;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.stages = pkv_dev::kTcStages;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (prefill_path_tc() && n_seqs <= kPrefillTcMaxSeqs) {
+    // tensor-core path: tcgen05.mma with accumulators in tensor memory, 128-row tiles
+    using TK = void (*)(pkv_dev::PrefillArgs, pkv_dev::TcMaps);
+    TK kern = nullptr;
+    size_t smem = 0;
+    int tq = 0;
+#define PKV_TC_CASE(DD, GG)                                            \
+    if (d.head_dim == DD && g == GG) {                                 \
+      kern = pkv_dev::paged_prefill_tc_kernel<DD, GG>;                 \
+      smem = pkv_dev::prefill_tc_smem_bytes<DD, GG>(n_seqs);           \
+      tq = pkv_dev::TcShape<DD, GG>::TQ;                               \
+    }
+    PKV_TC_CASE(64, 1) PKV_TC_CASE(64, 2) PKV_TC_CASE(64, 3) PKV_TC_CASE(64, 4)
+    PKV_TC_CASE(64, 5) PKV_TC_CASE(64, 6) PKV_TC_CASE(64, 7) PKV_TC_CASE(64, 8)
+    PKV_TC_CASE(128, 1) PKV_TC_CASE(128, 2) PKV_TC_CASE(128, 3) PKV_TC_CASE(128, 4)
+    PKV_TC_CASE(128, 5) PKV_TC_CASE(128, 6) PKV_TC_CASE(128, 7) PKV_TC_CASE(128, 8)
+#undef PKV_TC_CASE
+    if (!kern) return PKV_ERR_INVALID;
+    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return PKV_ERR_CUDA;
+    pkv_dev::TcMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d) ||
+        !encode_q_map(&maps.q, q, total_q, num_q_heads, d.head_dim, g))
+      return PKV_ERR_CUDA;
+    const int64_t tiles_ub = (static_cast<int64_t>(total_q) + tq - 1) / tq + n_seqs;   // >= sum of tiles
+    if (tiles_ub > 0x7fffffffLL) return PKV_ERR_INVALID;
+    if (launch(kern, dim3(static_cast<unsigned>(tiles_ub), d.num_kv_heads), dim3(pkv_dev::kTcThreads), smem, st, a,
+               maps) != cudaSuccess ||
+        cudaGetLastError() != cudaSuccess)
+      return PKV_ERR_CUDA;
+    return PKV_OK;
+  }
   using PK = void (*)(pkv_dev::PrefillArgs, pkv_dev::TmaMaps);
   PK kern = nullptr;
   int tq = 0, stage_bytes = 0, q_bytes = 0;
@@ -450,30 +523,14 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   const int stages = env_int("PKV_PREFILL_STAGES", 4);
   const size_t smem = pkv_dev::prefill_smem_bytes(stages, stage_bytes, q_bytes, n_seqs, d.max_blocks_per_seq);
   if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return PKV_ERR_CUDA;
-  const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size;
-  if (rows > 0x7fffffffLL) return PKV_ERR_INVALID;
   pkv_dev::TmaMaps maps;
   std::memset(&maps, 0, sizeof maps);
   if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d)) return PKV_ERR_CUDA;
-  pkv_dev::PrefillArgs a;
-  a.out = out;
-  a.q = q;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.cu_q = cu_q;
-  a.n_seqs = n_seqs;
-  a.Hq = num_q_heads;
-  a.Hkv = d.num_kv_heads;
-  a.B = d.block_size;
-  a.NB = d.num_blocks;
-  a.MB = d.max_blocks_per_seq;
-  a.window = window;
   a.stages = stages;
-  a.scale_log2 = scale * 1.4426950408889634f;
   const int64_t tiles_ub = (static_cast<int64_t>(total_q) + tq - 1) / tq + n_seqs;   // >= sum of tiles
-  if (tiles_ub > 0x7fffffffLL || d.num_kv_heads > 65535) return PKV_ERR_INVALID;
-  if (launch(kern, dim3(static_cast<unsigned>(tiles_ub), d.num_kv_heads), dim3(128), smem,
-             static_cast<cudaStream_t>(stream), a, maps) != cudaSuccess ||
+  if (tiles_ub > 0x7fffffffLL) return PKV_ERR_INVALID;
+  if (launch(kern, dim3(static_cast<unsigned>(tiles_ub), d.num_kv_heads), dim3(128), smem, st, a, maps) !=
+          cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;

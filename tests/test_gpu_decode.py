@@ -286,3 +286,31 @@ def test_largest_batch_and_the_shared_memory_limit():
         c.gpu_decode(64, window=24)
     assert e.value.status == pkv.ERR_INVALID
     assert pkv.last_error() == pkv.OK
+
+
+@pytest.mark.parametrize("pt", [0, 512, 64])
+def test_cuda_graph_replays_match_direct_calls_bitwise(pt, path):
+    """A decode captured in a CUDA graph and replayed several times returns exactly what a direct
+    call returns: a replay launches with the captured call's arguments (the same arrival-counter
+    tag included), so the counters must start from zero again on every replay."""
+    c = case_from_workload("gqa5_bf16", host_cache=False)
+    ref = c.gpu_decode(pt)
+    nbytes = c.pool.decode_workspace_bytes(c.n, c.Hq, pt)
+    ws = torch.full((max(nbytes, 16) // 4 + 4,), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full_like(ref, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):                      # a direct call of the same shape first
+        c.pool.paged_decode(out, c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale,
+                            partition_tokens=pt, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        c.pool.paged_decode(out, c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale,
+                            partition_tokens=pt, workspace=ws)
+    for _ in range(4):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert pkv.last_error() == pkv.OK

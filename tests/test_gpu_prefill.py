@@ -17,6 +17,24 @@ from tests.gpu_cases import Case, to_device
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["tc", "mma"], autouse=True)
+def path(request, monkeypatch):
+    """Every prefill test runs on both kernels: tcgen05 (the default) and mma.sync."""
+    if request.param == "mma":
+        monkeypatch.setenv("PKV_PREFILL_PATH", "mma")
+    else:
+        monkeypatch.delenv("PKV_PREFILL_PATH", raising=False)
+    return request.param
+
+
+def test_single_tile_one_kv_head():
+    """The smallest case: one CTA (32 query tokens x 4 heads = 128 rows), one 32-key tile."""
+    c = Case(lengths=[32], Hq=4, Hkv=1, D=128, B=16, dtype="bf16", seed=3)
+    out, ref, _, _ = run_prefill(c, [32])
+    assert max_err(out, ref) <= 2e-3
+    assert pkv.last_error() == pkv.OK
+
+
 def run_prefill(c: Case, qlens, window=0, seed=1):
     cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
     q_stored = synth.encode(synth.normal_f32((int(cu[-1]), c.Hq, c.D), seed, 55), "bf16")
@@ -35,7 +53,7 @@ def max_err(out, ref):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_prefill_shapes(D, G):
     lens = [1, 17, 100, 333, 64, 700, 40]
     qlens = [1, 17, 37, 333, 0, 5, 16]           # full prefill, partial chunks, empty, one token
@@ -86,3 +104,19 @@ def test_bad_query_counts_reported_not_faulted():
         f.pool.paged_prefill(torch.zeros(1, 2, 64, device="cuda"), torch.zeros(1, 2, 64, device="cuda"),
                              f.k_cache, f.v_cache, f.tables, f.lens, torch.tensor([0, 1], dtype=torch.int32,
                                                                                   device="cuda"), f.scale)
+
+
+def test_tensor_core_paths_agree(path, monkeypatch):
+    """The tcgen05 and mma.sync kernels on one problem with every tile shape at once: ragged query
+    tiles, keys past the context end in the last tile, many sequences."""
+    if path != "tc":
+        pytest.skip("compares both kernels once")
+    rng = np.random.default_rng(23)
+    lens = rng.integers(1, 600, size=40).tolist()
+    qlens = [int(rng.integers(0, L + 1)) for L in lens]
+    c = Case(lengths=lens, Hq=32, Hkv=8, D=128, B=16, dtype="bf16", seed=23)
+    out_tc, ref, _, _ = run_prefill(c, qlens)
+    monkeypatch.setenv("PKV_PREFILL_PATH", "mma")
+    out_mma, _, _, _ = run_prefill(c, qlens)
+    assert max_err(out_tc, ref) <= 2e-3 and max_err(out_mma, ref) <= 2e-3
+    assert float((out_tc - out_mma).abs().max()) <= 2e-3
