@@ -46,7 +46,7 @@ METRIC = "paged-decode KV GB/s read (% of B300 HBM peak); decode seq-steps/sec"
 FALLBACK_HBM_GBS = 6400.0
 NOMINAL_HBM_GBS = 7700.0      # B300 HBM3e datasheet figure (context beside the measured copy peak)
 L2_FLUSH_BYTES = 256 << 20    # a write of this many bytes evicts the 126 MB L2
-PREFILL_KERNEL = "paged_prefill_kernel (mma.sync m16n8k16, P as bf16 hi + lo)"
+PREFILL_KERNEL = "paged_prefill_tc_kernel (tcgen05.mma, S and O in tensor memory, P as bf16 hi + lo)"
 
 
 # ------------------------------------------------------------------------------------------------

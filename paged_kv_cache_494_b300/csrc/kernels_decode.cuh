@@ -731,7 +731,7 @@ struct MmaMath {
 // is carried as f16 hi + lo (paired columns as in the bf16 path); the running max is raised when a
 // chunk exceeds it by 2^2, so p <= 4 and P' stays inside the f16 normal range for |V| < ~7000.
 // ------------------------------------------------------------------------------------------------
-template <int G>
+template <int G, int kCtas = 3>
 struct Fp8Math {
   static_assert(G >= 1 && G <= 8, "G <= 8");
   static constexpr int D = 128;
@@ -740,7 +740,7 @@ struct Fp8Math {
   static constexpr int kScaleOff = KBOX + VBOX;
   static constexpr int kTxBytes = KBOX + VBOX + 2 * kChunk * 4;
   static constexpr int kStageBytes = 5120;
-  static constexpr int kMinCtasPerSm = 3;
+  static constexpr int kMinCtasPerSm = kCtas;   // resident CTAs per SM the register budget is cut for
   static constexpr int KS = D / 16;          // k-steps of q.K and m-tiles of p.V
   static constexpr bool kPaired = G <= 4;
   static constexpr float kRescaleLog2 = 2.f;

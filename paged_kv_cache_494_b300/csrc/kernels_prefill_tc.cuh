@@ -8,20 +8,26 @@
 // `window` positions) through the block table.
 //
 // Decomposition (B300 design):
-//  * One CTA per 128-row tile of one KV head: row r = (query token r / G, query head r % G of the
-//    GQA group), 128 / G query tokens per CTA, so every staged K/V byte feeds 128 rows. Tiles of a
-//    sequence are dispatched from its last (longest causal range) to its first.
-//  * 6 warps. Warp 4 (one lane) issues TMA copies: the Q tile once (3-D tensor map over
-//    [token][head][dim], 128-byte swizzle), then 32-key K and V tiles through a ring of 3 stages,
-//    16 keys (one block piece) per copy, chunks outside the causal range filled with zeros by
-//    out-of-range coordinates. Warp 5 allocates tensor memory and one lane issues the MMAs.
-//    Warps 0-3 own one row each per thread (tensor-memory lane = row): softmax and the epilogue.
-//  * Per 32-key tile j: S_j = Q K_j^T (M 128, N 32, K = D; into one of two S buffers in tensor
-//    memory, so S_{j+1} is computed while S_j is in softmax); the softmax threads load their row of
-//    S_j, apply the causal / window mask and the running max (raised only when a tile exceeds it by
-//    2^8, so rescales of O are rare), and write P_j to shared memory as bf16 hi and the bf16 rounding
-//    of the remainder lo, side by side in one 128-byte row ([hi keys 0..31][lo keys 0..31]); then
-//    O += P V_j is one MMA chain over K = 64 (hi against V, then lo against the same V), so P keeps
+//  * A Q tile is 128 rows of one KV head: row r = (query token r / G, query head r % G of the GQA
+//    group), 128 / G query tokens. One CTA owns NT consecutive Q tiles of a sequence (NT = 2 for the
+//    large shapes: every staged K/V byte then feeds 256 rows, and the two tiles' softmax and MMA
+//    chains interleave on the tensor core). Work items of a sequence are dispatched from the last
+//    (longest causal range) to the first.
+//  * Warps 0 .. 4NT-1: softmax and epilogue, one row per thread (warp w serves tile w / 4, tensor-
+//    memory lanes 32 (w % 4) ..). Warp 4NT issues TMA copies (one lane; the warp reads block-table
+//    entries 32 at a time and hands them over by shuffle): the Q tiles once (3-D tensor map over
+//    [token][head][dim], 128-byte swizzle), then 64-key K and V steps of the union of the tiles'
+//    causal ranges through a ring of STAGES stages, 16 keys (one block piece) per copy, chunks
+//    outside the range filled with zeros by out-of-range coordinates; the copies of a step are issued
+//    by 16 lanes at once (a tensor copy costs ~100 cycles to issue). Per tile, one lane of one warp
+//    issues the S MMAs and one lane of another the O += P V MMAs, so no chain waits on another's
+//    inputs (a tcgen05.mma costs tens of cycles to issue). The first S warp allocates tensor memory.
+//  * Per tile and 64-key step i: S_i = Q K_i^T (M 128, N 64, K = D) into one of two S buffers of the
+//    tile in tensor memory, so S_{i+1} is computed while S_i is in softmax; the softmax threads load
+//    their row of S_i, apply the causal / window mask and the running max (raised only when a step
+//    exceeds it by 2^8, so rescales of O are rare), and write P_i to shared memory as bf16 hi (keys
+//    0..63, one 128-byte row) and the bf16 rounding of the remainder lo (a second 128-byte row); then
+//    O += P V_i is one MMA chain over K = 128 (hi against V, then lo against the same V), so P keeps
 //    ~17 bits and the O accumulator (f32, tensor memory) sees the exact-attention weights.
 //  * Every wait is bounded (pkv_device.cuh); a role that gives up sets a shared abort flag, every
 //    role stops, the producer waits for its copies in flight, the MMA lane for its MMAs, and the
@@ -33,38 +39,47 @@
 
 namespace pkv_dev {
 
-constexpr int kTcRows = 128;   // M of every MMA: rows of one CTA
-constexpr int kTcKeys = 32;    // keys per tile: N of S = Q K^T, half the K of O += P V
-constexpr int kTcStages = 3;   // K/V ring depth
-constexpr int kTcThreads = 192;
+constexpr int kTcRows = 128;   // M of every MMA: rows of one Q tile
+constexpr int kTcKeys = 64;    // keys per step: N of S = Q K^T, half the K of O += P V
+constexpr int kTcChunks = kTcKeys / kChunk;   // 16-key block pieces per step
 
-template <int D, int G>
+template <int D, int G, int NT, int STAGES>
 struct TcShape {
-  static constexpr int TQ = kTcRows / G;            // query tokens per CTA
+  static constexpr int TQ = kTcRows / G;            // query tokens per Q tile
   static constexpr int ROWS = TQ * G;               // real rows (128 or slightly fewer)
+  // warps: 4NT softmax, 1 producer, then per tile one S-issuing and one PV-issuing warp
+  static constexpr int THREADS = 128 * NT + 32 * (1 + 2 * NT);
+  static constexpr int PRODUCER = 4 * NT;
+  static constexpr int MMA = 4 * NT + 1;            // S MMAs of tile 0 (warp MMA + t: tile t); allocates tensor memory
+  static constexpr int MMA_PV = 4 * NT + 1 + NT;    // O += P V MMAs of tile 0 (MMA_PV + t: tile t)
   static constexpr int DH = D / 64;                 // 128-byte halves of a D-wide row
-  static constexpr int Q_REGION = kTcRows * 128;    // one D half of the Q tile (16 KB)
-  static constexpr int Q_BYTES = DH * Q_REGION;
-  static constexpr int KV_REGION = kTcKeys * 128;   // one D half of a K (or V) tile (4 KB)
+  static constexpr int Q_REGION = kTcRows * 128;    // one D half of a Q tile (16 KB)
+  static constexpr int Q_TILE = DH * Q_REGION;
+  static constexpr int KV_REGION = kTcKeys * 128;   // one D half of a K (or V) step (8 KB)
   static constexpr int K_BYTES = DH * KV_REGION;
-  static constexpr int STAGE_BYTES = 2 * K_BYTES;   // K tile, then V tile
-  static constexpr int P_BYTES = kTcRows * 128;     // [row][hi keys 0..31 | lo keys 0..31] bf16
-  static constexpr int S_COL = D;                   // tensor-memory columns: O at 0..D-1, S at D, D+32
-  static constexpr uint32_t TMEM_COLS = (D + 2 * kTcKeys) <= 128 ? 128u : 256u;
+  static constexpr int STAGE_BYTES = 2 * K_BYTES;   // K step, then V step
+  static constexpr int P_REGION = kTcRows * 128;    // 128 rows x 128 bytes: 64 keys of bf16
+  static constexpr int P_BYTES = 2 * P_REGION;      // one tile's P: hi region, then lo region
+  static constexpr int TCOLS = D + 2 * kTcKeys;     // tensor-memory columns of a tile: O, then 2 S buffers
+  static constexpr uint32_t TMEM_COLS = NT * TCOLS <= 128 ? 128u : NT * TCOLS <= 256 ? 256u : 512u;
   static constexpr int KSTEPS = D / 16;             // k-steps of S = Q K^T
-  static constexpr int RING_OFF = Q_BYTES;
-  static constexpr int P_OFF = RING_OFF + kTcStages * STAGE_BYTES;
-  static constexpr int BAR_OFF = P_OFF + P_BYTES;
-  static constexpr int N_BARS = 1 + 2 * kTcStages + 2 + 2 + 1 + 1 + 1;
+  static constexpr int RING_OFF = NT * Q_TILE;
+  static constexpr int P_OFF = RING_OFF + STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = P_OFF + NT * P_BYTES;
+  // q_full, kv_full/empty[STAGES], per tile: s_full[2], s_free[2], p_full, pv_done; drain
+  static constexpr int N_BARS = 1 + 2 * STAGES + 6 * NT + 1;
+  static constexpr int SOFTMAX_THREADS = 128 * NT;
   static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;   // tmem base, abort flag, scan scratch, prefix
   static_assert(D == 64 || D == 128, "D");
   static_assert(G >= 1 && G <= 8, "G");
+  static_assert(NT == 1 || NT == 2, "NT");
+  static_assert(NT * TCOLS <= 512, "tensor memory");
 };
 
-// [1 KB alignment slack][Q][ring][P][barriers][tmem base, abort][64-int scan scratch][tile prefix]
-template <int D, int G>
+// [1 KB alignment slack][Q tiles][ring][P][barriers][tmem base, abort][64-int scan scratch][prefix]
+template <class Sh>
 __host__ __device__ inline size_t prefill_tc_smem_bytes(int n_seqs) {
-  return 1024 + TcShape<D, G>::MISC_OFF + 16 + 256 + static_cast<size_t>(n_seqs + 1) * 4;
+  return 1024 + Sh::MISC_OFF + 16 + 256 + static_cast<size_t>(n_seqs + 1) * 4;
 }
 
 // ---- tcgen05 primitives (one instruction each; syntax of the PTX ISA) ----------------------------
@@ -148,11 +163,11 @@ struct TcMaps {
   CUtensorMap q;
 };
 
-template <int D, int G>
-__global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const __grid_constant__ PrefillArgs a,
-                                                                        const __grid_constant__ TcMaps maps) {
-  using Sh = TcShape<D, G>;
-  constexpr int TQ = Sh::TQ, ROWS = Sh::ROWS, DH = Sh::DH;
+template <int D, int G, int NT, int STAGES>
+__global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
+    paged_prefill_tc_kernel(const __grid_constant__ PrefillArgs a, const __grid_constant__ TcMaps maps) {
+  using Sh = TcShape<D, G, NT, STAGES>;
+  constexpr int TQ = Sh::TQ, ROWS = Sh::ROWS, DH = Sh::DH, NTHR = Sh::THREADS;
   constexpr float kRescaleLog2 = 8.f;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t n = a.n_seqs;
@@ -164,12 +179,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Sh::BAR_OFF);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + kTcStages;
-  uint64_t* s_full = kv_empty + kTcStages;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* drain = pv_done + 1;
+  uint64_t* kv_empty = kv_full + STAGES;
+  uint64_t* tbar = kv_empty + STAGES;      // per tile t: tbar + 6t = s_full[2], s_free[2], p_full, pv_done
+  uint64_t* drain = tbar + 6 * NT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::MISC_OFF + 4);
   int32_t* wsum = reinterpret_cast<int32_t*>(smem + Sh::MISC_OFF + 16);
@@ -177,11 +189,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
 
   pdl_wait();   // before any global access, and before holding tensor memory
 
-  // ---- query-tile prefix over sequences (block-wide scan)
+  // ---- work-item prefix over sequences (block-wide scan); an item is NT Q tiles of a sequence
+  constexpr int ITEM = NT * TQ;             // query tokens per CTA
   {
-    const int nw = kTcThreads / 32;
+    constexpr int nw = NTHR / 32;
     int32_t carry = 0;
-    for (int32_t base = 0; base < n; base += kTcThreads) {
+    for (int32_t base = 0; base < n; base += NTHR) {
       const int32_t b = base + tid;
       int32_t c = 0;
       if (b < n) {
@@ -190,7 +203,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
           record_error(ERRBIT_BOUNDS);
           ql = 0;
         }
-        c = (ql + TQ - 1) / TQ;
+        c = (ql + ITEM - 1) / ITEM;
       }
       int32_t ic = c;
 #pragma unroll
@@ -212,8 +225,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
     if (tid == 0) tpref[n] = carry;
     __syncthreads();
   }
-  const int32_t tile = blockIdx.x;
-  if (tile >= tpref[n]) {
+  const int32_t item = blockIdx.x;
+  if (item >= tpref[n]) {
     pdl_launch_dependents();
     return;
   }
@@ -222,13 +235,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
     int32_t lo = 0, hi = n - 1;
     while (lo < hi) {
       const int32_t mid = (lo + hi + 1) >> 1;
-      if (tpref[mid] <= tile) lo = mid; else hi = mid - 1;
+      if (tpref[mid] <= item) lo = mid; else hi = mid - 1;
     }
     b = lo;
   }
   const int32_t h = blockIdx.y;
-  const int32_t n_qt = tpref[b + 1] - tpref[b];
-  const int32_t qt = n_qt - 1 - (tile - tpref[b]);          // longest causal ranges first
+  const int32_t qt = (tpref[b + 1] - tpref[b]) - 1 - (item - tpref[b]);   // longest causal ranges first
   int32_t len = __ldg(a.context_lens + b);
   const int32_t cap = a.MB * a.B;
   if (len < 0 || len > cap) {
@@ -241,45 +253,60 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
     if (tid == 0) record_error(ERRBIT_BOUNDS);
     ql = len;
   }
-  const int32_t t_begin = qt * TQ;
-  const int32_t t_end = min(t_begin + TQ, ql);
+  const int32_t t_begin = qt * ITEM;                  // first query token of this CTA
+  const int32_t t_end = min(t_begin + ITEM, ql);      // one past its last
   if (t_begin >= t_end) {
     pdl_launch_dependents();
     return;
   }
   const int32_t pos0 = len - ql;
-  const int32_t p_lo = pos0 + t_begin, p_hi = pos0 + t_end - 1;
-  const int32_t c_lo = (a.window > 0 && p_lo - a.window + 1 > 0) ? (p_lo - a.window + 1) / kChunk : 0;
-  const int32_t c_hi = p_hi / kChunk;
-  const int32_t kt_lo = c_lo / 2, kt_hi = c_hi / 2;          // 32-key tiles = 2 chunks of 16
-  const int32_t n_tiles = kt_hi - kt_lo + 1;
-  const int32_t ws_max = a.window > 0 ? p_hi - a.window + 1 : 0;   // latest window start in the CTA
+  const int n_act = (t_end - t_begin + TQ - 1) / TQ;  // Q tiles with tokens (1 .. NT)
+  // key range of the CTA (the union of its tiles' ranges) in 16-key chunks and 32-key steps
+  const int32_t c_lo = (a.window > 0 && pos0 + t_begin - a.window + 1 > 0) ? (pos0 + t_begin - a.window + 1) / kChunk : 0;
+  const int32_t c_hi = (pos0 + t_end - 1) / kChunk;
+  const int32_t kt_lo = c_lo / kTcChunks, kt_hi = c_hi / kTcChunks;
+  const int32_t n_steps = kt_hi - kt_lo + 1;
+  // step range of tile t: [kt_lo + off[t], kt_lo + off[t] + cnt[t])
+  auto tile_first_tok = [&](int t) { return t_begin + t * TQ; };
+  auto tile_last_tok = [&](int t) { return min(t_begin + (t + 1) * TQ, t_end) - 1; };
+  auto tile_off = [&](int t) -> int32_t {
+    const int32_t p = pos0 + tile_first_tok(t);
+    const int32_t c = (a.window > 0 && p - a.window + 1 > 0) ? (p - a.window + 1) / kChunk : 0;
+    return c / kTcChunks - kt_lo;
+  };
+  auto tile_cnt = [&](int t) -> int32_t {
+    return (pos0 + tile_last_tok(t)) / kChunk / kTcChunks - kt_lo - tile_off(t) + 1;
+  };
 
   // ---- barriers, tensor memory, padding rows of Q
-  if (tid == 32 * 4) {
+  if (tid == 32 * Sh::PRODUCER) {
     mbar_init(smem_addr(q_full), 1);
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_addr(kv_full + s), 1);
-      mbar_init(smem_addr(kv_empty + s), 1);
+      mbar_init(smem_addr(kv_empty + s), NT);   // one arrival per PV-issuing lane
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(s_full + s), 1);
-      mbar_init(smem_addr(s_free + s), 4);
+    for (int t = 0; t < NT; ++t) {
+      uint64_t* tb = tbar + 6 * t;
+      mbar_init(smem_addr(tb + 0), 1);   // s_full[0..1]: one commit
+      mbar_init(smem_addr(tb + 1), 1);
+      mbar_init(smem_addr(tb + 2), 4);   // s_free[0..1]: one arrival per softmax warp
+      mbar_init(smem_addr(tb + 3), 4);
+      mbar_init(smem_addr(tb + 4), 4);   // p_full
+      mbar_init(smem_addr(tb + 5), 1);   // pv_done
     }
-    mbar_init(smem_addr(p_full), 4);
-    mbar_init(smem_addr(pv_done), 1);
-    mbar_init(smem_addr(drain), 1);
+    mbar_init(smem_addr(drain), 2 * NT);   // one commit from each MMA-issuing lane
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == Sh::MMA) {
     tmem_alloc(smem_addr(tmem_slot), Sh::TMEM_COLS);
     tmem_relinquish();
   }
-  if constexpr (ROWS < kTcRows) {   // rows the Q copy does not write: zeros (their results are dropped)
-    for (int i = tid; i < (kTcRows - ROWS) * 8 * DH; i += kTcThreads) {
-      const int dh = i / ((kTcRows - ROWS) * 8), rem = i % ((kTcRows - ROWS) * 8);
-      *reinterpret_cast<uint4*>(smem + dh * Sh::Q_REGION + (ROWS + rem / 8) * 128 + (rem % 8) * 16) =
+  if constexpr (ROWS < kTcRows) {   // rows the Q copies do not write: zeros (their results are dropped)
+    constexpr int PER = (kTcRows - ROWS) * 8;   // 16-byte pieces per D half
+    for (int i = tid; i < NT * DH * PER; i += NTHR) {
+      const int reg = i / PER, rem = i % PER;   // reg = tile * DH + dh
+      *reinterpret_cast<uint4*>(smem + reg * Sh::Q_REGION + (ROWS + rem / 8) * 128 + (rem % 8) * 16) =
           make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
@@ -289,137 +316,189 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
-    // ================= producer: TMA copies (one lane) =================
-    if (lane == 0) {
-      const uint64_t policy = policy_evict_first();
-      mbar_arrive_expect_tx(smem_addr(q_full), DH * ROWS * 128);
-#pragma unroll
-      for (int dh = 0; dh < DH; ++dh)
-        tma_load_3d(q_s + dh * Sh::Q_REGION, &maps.q, 64 * dh, h * G, q0 + t_begin, smem_addr(q_full));
-      int32_t issued = 0;
-      for (int32_t j = 0; j < n_tiles; ++j) {
-        const int s = j % kTcStages;
-        if (j >= kTcStages &&
-            !mbar_wait_bounded(smem_addr(kv_empty + s), static_cast<uint32_t>(((j / kTcStages) - 1) & 1))) {
+  if (warp == Sh::PRODUCER) {
+    // ================= producer: TMA copies (lane 0 issues; the warp reads the block table) =========
+    const uint64_t policy = policy_evict_first();
+    if (lane == 0) mbar_arrive_expect_tx(smem_addr(q_full), n_act * DH * ROWS * 128);
+    __syncwarp();
+    if (lane < n_act * DH) {   // one Q box per lane: tile lane / DH, D half lane % DH
+      const int t = lane / DH, dh = lane % DH;
+      tma_load_3d(q_s + (t * DH + dh) * Sh::Q_REGION, &maps.q, 64 * dh, h * G, q0 + tile_first_tok(t),
+                  smem_addr(q_full));
+    }
+    const int32_t* table = a.block_tables + static_cast<int64_t>(b) * a.MB;
+    constexpr int BOXES = kTcChunks * 2 * DH;           // copies of one step: chunk x (K, V) x D half
+    const int my_c = lane / (2 * DH), my_kv = (lane / DH) & 1, my_dh = lane % DH;   // lane < BOXES
+    int32_t win_base = -1 << 30, win_val = -1;
+    int32_t issued = 0;
+    for (int32_t j = 0; j < n_steps; ++j) {
+      const int s = j % STAGES;
+      int stop = 0;
+      if (lane == 0) {
+        if (j >= STAGES &&
+            !mbar_wait_bounded(smem_addr(kv_empty + s), static_cast<uint32_t>(((j / STAGES) - 1) & 1)))
           *abort_flag = 1;
-          break;
-        }
-        if (*abort_flag) break;
-        const uint32_t kst = ring_s + s * Sh::STAGE_BYTES, vst = kst + Sh::K_BYTES;
-        const uint32_t bar = smem_addr(kv_full + s);
-        mbar_arrive_expect_tx(bar, Sh::STAGE_BYTES);
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int32_t ci = (kt_lo + j) * 2 + c;            // 16-key chunk of the sequence
-          int32_t y = -kChunk;                               // fully out of range: zero fill
-          if (ci >= c_lo && ci <= c_hi) {
-            const int32_t tok0 = ci * kChunk;
-            const int32_t pg = tok0 / a.B;
-            const int32_t blk = __ldg(a.block_tables + static_cast<int64_t>(b) * a.MB + pg);
-            if (blk >= 0 && blk < a.NB)
-              y = static_cast<int32_t>((static_cast<int64_t>(blk) * a.Hkv + h) * a.B + (tok0 - pg * a.B));
-            else
-              record_error(ERRBIT_BOUNDS);
-          }
-#pragma unroll
-          for (int dh = 0; dh < DH; ++dh) {
-            tma_load_2d(kst + dh * Sh::KV_REGION + c * (kChunk * 128), &maps.k, 64 * dh, y, bar, policy);
-            tma_load_2d(vst + dh * Sh::KV_REGION + c * (kChunk * 128), &maps.v, 64 * dh, y, bar, policy);
-          }
-        }
-        issued = j + 1;
+        stop = *abort_flag;
       }
+      if (__shfl_sync(0xffffffffu, stop, 0)) break;
+      const uint32_t bar = smem_addr(kv_full + s);
+      // block-table entries of the step's chunks: window of 32 pages, one per lane
+      const int32_t pg0 = (kt_lo + j) * kTcKeys / a.B;
+      const int32_t pg_last = ((kt_lo + j) * kTcKeys + kTcKeys - 1) / a.B;
+      if (pg0 < win_base || pg_last >= win_base + 32) {
+        win_base = pg0;
+        win_val = pg0 + lane < a.MB ? __ldg(table + pg0 + lane) : -1;
+      }
+      const int32_t ci = (kt_lo + j) * kTcChunks + my_c;   // this lane's 16-key chunk
+      const int32_t pg = ci * kChunk / a.B;
+      const int32_t blk = __shfl_sync(0xffffffffu, win_val, min(max(pg - win_base, 0), 31));
+      if (lane == 0) mbar_arrive_expect_tx(bar, Sh::STAGE_BYTES);
+      __syncwarp();
+      if (lane < BOXES) {
+        int32_t y = -kChunk;                                  // fully out of range: zero fill
+        if (ci >= c_lo && ci <= c_hi) {
+          if (blk >= 0 && blk < a.NB)
+            y = static_cast<int32_t>((static_cast<int64_t>(blk) * a.Hkv + h) * a.B + (ci * kChunk - pg * a.B));
+          else if (my_kv == 0 && my_dh == 0)
+            record_error(ERRBIT_BOUNDS);
+        }
+        const uint32_t dst = ring_s + s * Sh::STAGE_BYTES + my_kv * Sh::K_BYTES + my_dh * Sh::KV_REGION +
+                             my_c * (kChunk * 128);
+        tma_load_2d(dst, my_kv ? &maps.v : &maps.k, 64 * my_dh, y, bar, policy);
+      }
+      issued = j + 1;
+    }
+    if (lane == 0) {
       // drain: the last copy issued into each stage (and Q) has landed before the CTA may leave
       mbar_wait_bounded(smem_addr(q_full), 0u);
-      for (int s = 0; s < kTcStages; ++s) {
-        const int32_t cnt = issued > s ? (issued - 1 - s) / kTcStages + 1 : 0;   // copies into stage s
+      for (int s = 0; s < STAGES; ++s) {
+        const int32_t cnt = issued > s ? (issued - 1 - s) / STAGES + 1 : 0;   // copies into stage s
         if (cnt > 0) mbar_wait_bounded(smem_addr(kv_full + s), static_cast<uint32_t>((cnt - 1) & 1));
       }
     }
-  } else if (warp == 5) {
-    // ================= MMA issue (one lane) =================
+  } else if (warp >= Sh::MMA) {
+    // ================= MMA issue: S of tile t on warp MMA + t, O += P V on warp MMA_PV + t =========
     if (lane == 0) {
       constexpr uint32_t idesc_s = pkv_umma::idesc_bf16_f32(kTcRows, kTcKeys, false, false);
       constexpr uint32_t idesc_pv = pkv_umma::idesc_bf16_f32(kTcRows, D, false, true);
       static_assert(pkv_umma::valid_f16_shape(kTcRows, kTcKeys) && pkv_umma::valid_f16_shape(kTcRows, D), "shape");
-      bool ok = mbar_wait_bounded(smem_addr(q_full), 0u);
-      auto pv = [&](int32_t i) -> bool {   // O += P_i V_i
-        if (!mbar_wait_bounded(smem_addr(p_full), static_cast<uint32_t>(i & 1))) return false;
-        tc_fence_after();
-        const uint32_t vst = ring_s + (i % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES;
+      const bool is_s = warp < Sh::MMA_PV;
+      const int t = is_s ? warp - Sh::MMA : warp - Sh::MMA_PV;
+      const int32_t off = t < n_act ? tile_off(t) : 0, cnt = t < n_act ? tile_cnt(t) : 0;
+      uint64_t* tb = tbar + 6 * t;
+      bool ok = true;
+      if (is_s) {
+        ok = mbar_wait_bounded(smem_addr(q_full), 0u);
+        const uint32_t qt_s = q_s + t * Sh::Q_TILE;
+        for (int32_t i = 0; ok && i < cnt; ++i) {   // S of step i of tile t (ring step off + i)
+          const int32_t j = off + i;
+          const int sb = i & 1;
+          if (!mbar_wait_bounded(smem_addr(kv_full + j % STAGES), static_cast<uint32_t>((j / STAGES) & 1)) ||
+              (i >= 2 && !mbar_wait_bounded(smem_addr(tb + 2 + sb), static_cast<uint32_t>(((i >> 1) - 1) & 1))) ||
+              *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kst = ring_s + (j % STAGES) * Sh::STAGE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {   // keys 0-15, 16-31 of hi, then of lo
-          const uint64_t ad = pkv_umma::smem_desc(p_s + kk * 32, 16, 1024, pkv_umma::kSwizzle128B);
-          const uint64_t bd =
-              pkv_umma::smem_desc(vst + (kk & 1) * (16 * 128), Sh::KV_REGION, 1024, pkv_umma::kSwizzle128B);
-          umma_f16(tmem, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < Sh::KSTEPS; ++kk) {
+            const uint32_t dh = (kk >> 2), col = (kk & 3) * 32;
+            const uint64_t ad =
+                pkv_umma::smem_desc(qt_s + dh * Sh::Q_REGION + col, 16, 1024, pkv_umma::kSwizzle128B);
+            const uint64_t bd =
+                pkv_umma::smem_desc(kst + dh * Sh::KV_REGION + col, 16, 1024, pkv_umma::kSwizzle128B);
+            umma_f16(tmem + t * Sh::TCOLS + D + kTcKeys * sb, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(smem_addr(tb + sb));
         }
-        tc_commit(smem_addr(kv_empty + (i % kTcStages)));
-        tc_commit(smem_addr(pv_done));
-        return true;
-      };
-      int32_t j = 0;
-      for (; ok && j < n_tiles; ++j) {
-        const int s = j % kTcStages, sb = j & 1;
-        if (!mbar_wait_bounded(smem_addr(kv_full + s), static_cast<uint32_t>((j / kTcStages) & 1)) ||
-            (j >= 2 && !mbar_wait_bounded(smem_addr(s_free + sb), static_cast<uint32_t>(((j >> 1) - 1) & 1))) ||
-            *abort_flag) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t kst = ring_s + s * Sh::STAGE_BYTES;
+      } else {
+        // every step of the ring gets one arrival from this lane on kv_empty: after its MMAs when the
+        // tile uses the step, otherwise a plain arrival once the stage's previous phase has completed
+        const uint32_t pst = p_s + t * Sh::P_BYTES;
+        for (int32_t j = 0; ok && j < n_steps; ++j) {
+          const int32_t i = j - off;
+          if (i >= 0 && i < cnt) {
+            if (!mbar_wait_bounded(smem_addr(tb + 4), static_cast<uint32_t>(i & 1)) || *abort_flag) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vst = ring_s + (j % STAGES) * Sh::STAGE_BYTES + Sh::K_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < Sh::KSTEPS; ++kk) {
-          const uint32_t off = (kk >> 2), col = (kk & 3) * 32;
-          const uint64_t ad = pkv_umma::smem_desc(q_s + off * Sh::Q_REGION + col, 16, 1024, pkv_umma::kSwizzle128B);
-          const uint64_t bd = pkv_umma::smem_desc(kst + off * Sh::KV_REGION + col, 16, 1024, pkv_umma::kSwizzle128B);
-          umma_f16(tmem + Sh::S_COL + kTcKeys * sb, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(smem_addr(s_full + sb));
-        if (j >= 1 && !pv(j - 1)) {
-          ok = false;
-          break;
+            for (int kk = 0; kk < 2 * kTcKeys / 16; ++kk) {   // keys 16q..16q+15 of hi (kk < 4), then of lo
+              const int q = kk & 3;
+              const uint64_t ad =
+                  pkv_umma::smem_desc(pst + (kk >> 2) * Sh::P_REGION + q * 32, 16, 1024, pkv_umma::kSwizzle128B);
+              const uint64_t bd =
+                  pkv_umma::smem_desc(vst + q * (16 * 128), Sh::KV_REGION, 1024, pkv_umma::kSwizzle128B);
+              umma_f16(tmem + t * Sh::TCOLS, ad, bd, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(smem_addr(tb + 5));
+            tc_commit(smem_addr(kv_empty + j % STAGES));
+          } else {
+            // the arrival must land in step j's phase: wait until the stage's previous phase is over
+            if (j >= STAGES &&
+                !mbar_wait_bounded(smem_addr(kv_empty + j % STAGES), static_cast<uint32_t>(((j / STAGES) - 1) & 1))) {
+              ok = false;
+              break;
+            }
+            mbar_arrive(smem_addr(kv_empty + j % STAGES));
+          }
         }
       }
-      if (ok && !pv(n_tiles - 1)) ok = false;
       if (!ok) *abort_flag = 1;
-      // every MMA issued has completed before tensor memory is read for the last time or freed
+      // every MMA this lane issued has completed before tensor memory is read for the last time or freed
       tc_commit(smem_addr(drain));
       mbar_wait_bounded(smem_addr(drain), 0u);
     }
   } else {
-    // ================= softmax and epilogue: thread tid owns row tid =================
-    const int r = tid;
-    const int32_t tok = min(t_begin + r / G, t_end - 1);      // padding rows repeat a real token
-    const bool row_real = r < ROWS && t_begin + r / G < t_end;
+    // ================= softmax and epilogue: thread owns row r of tile t =================
+    const int t = warp >> 2, r = tid & 127;
+    uint64_t* tb = tbar + 6 * t;
+    const bool active = t < n_act;
+    const int32_t first = tile_first_tok(t), last = active ? tile_last_tok(t) : first;
+    const int32_t tok = min(first + r / G, last);               // padding rows repeat a real token
+    const bool row_real = active && r < ROWS && first + r / G <= last;
     const int32_t p_r = pos0 + tok;
     const int32_t ws_r = a.window > 0 ? p_r - a.window + 1 : 0;
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * warp) << 16;
+    const int32_t p_min = pos0 + first;                          // smallest position of the tile
+    const int32_t ws_max = a.window > 0 ? pos0 + last - a.window + 1 : 0;
+    const int32_t t_off = active ? tile_off(t) : 0, t_cnt = active ? tile_cnt(t) : 0;
+    const uint32_t tm = tmem + t * Sh::TCOLS + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int32_t j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait_bounded(smem_addr(s_full + sb), static_cast<uint32_t>((j >> 1) & 1)) || *abort_flag) {
+    for (int32_t i = 0; i < t_cnt; ++i) {
+      const int sb = i & 1;
+      if (!mbar_wait_bounded(smem_addr(tb + sb), static_cast<uint32_t>((i >> 1) & 1)) || *abort_flag) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[32];
-      tmem_ld32(tmem + lane_addr + Sh::S_COL + kTcKeys * sb, s);
+      float s[kTcKeys];
+      {
+        float h0[32], h1[32];
+        tmem_ld32(tm + D + kTcKeys * sb, h0);
+        tmem_ld32(tm + D + kTcKeys * sb + 32, h1);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          s[k] = h0[k];
+          s[32 + k] = h1[k];
+        }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(s_free + sb));
-      const int32_t kbase = (kt_lo + j) * kTcKeys;
-      const bool full = kbase >= ws_max && kbase + kTcKeys - 1 <= p_lo;   // no key of the tile is masked
+      if (lane == 0) mbar_arrive(smem_addr(tb + 2 + sb));
+      const int32_t step = t_off + i;                               // step index in the CTA's ring
+      const int32_t kbase = (kt_lo + step) * kTcKeys;
+      const bool full = kbase >= ws_max && kbase + kTcKeys - 1 <= p_min;   // no key of the step is masked
       float mx = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, s[k]);
+        for (int k = 0; k < kTcKeys; ++k) mx = fmaxf(mx, s[k]);
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < kTcKeys; ++k) {
           const int32_t key = kbase + k;
           if (!(key <= p_r && key >= ws_r)) s[k] = -INFINITY;   // select, never multiply: s may be NaN
           mx = fmaxf(mx, s[k]);
@@ -432,9 +511,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
       m = mnew;
       const float msafe = m == -INFINITY ? 0.f : m;               // a row with no key yet: weights 0
       float sum = 0.f;
-      uint32_t hi[16], lo[16];
+      uint32_t hi[kTcKeys / 2], lo[kTcKeys / 2];
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
+      for (int k = 0; k < kTcKeys; k += 2) {
         const float p0 = exp2f(fmaf(s[k], a.scale_log2, -msafe));
         const float p1 = exp2f(fmaf(s[k + 1], a.scale_log2, -msafe));
         sum += p0 + p1;
@@ -443,9 +522,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
         lo[k / 2] = pack_bf16x2(p0 - bf16_lo(hw), p1 - bf16_hi(hw));
       }
       l = l * alpha + sum;
-      // P_j may overwrite P_{j-1} and O may be rescaled only once O += P_{j-1} V_{j-1} has completed
-      if (j > 0) {
-        if (!mbar_wait_bounded(smem_addr(pv_done), static_cast<uint32_t>((j - 1) & 1))) {
+      // P_i overwrites P_{i-1}, and O may be rescaled, only once O += P_{i-1} V has completed
+      if (i > 0) {
+        if (!mbar_wait_bounded(smem_addr(tb + 5), static_cast<uint32_t>((i - 1) & 1))) {
           ok = false;
           *abort_flag = 1;
           break;
@@ -455,31 +534,32 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
             float o[32];
-            tmem_ld32(tmem + lane_addr + c, o);
+            tmem_ld32(tm + c, o);
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] *= alpha;
-            tmem_st32(tmem + lane_addr + c, o);
+            tmem_st32(tm + c, o);
           }
           tmem_wait_st();
         }
       }
-      // P row: 16-byte chunk c (c < 4: hi keys 8c..8c+7; c >= 4: lo keys 8(c-4)..) at c ^ (r & 7)
-      unsigned char* prow = smem + Sh::P_OFF + r * 128;
+      // P rows: hi region, then lo region; 16-byte chunk c (keys 8c..8c+7) of row r at c ^ (r & 7)
+      unsigned char* prow = smem + Sh::P_OFF + t * Sh::P_BYTES + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 8; ++c) {
         *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
             make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-        *reinterpret_cast<uint4*>(prow + (((c + 4) ^ (r & 7)) << 4)) =
+        *reinterpret_cast<uint4*>(prow + Sh::P_REGION + ((c ^ (r & 7)) << 4)) =
             make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
       }
       // keys at or past the context end may hold anything (even NaN) in the staged V: zero them
+      // (every tile using the step writes the same zeros before its own O += P V)
       if (kbase + kTcKeys > len) {
-        const int s = j % kTcStages;
-        mbar_wait_bounded(smem_addr(kv_full + s), static_cast<uint32_t>((j / kTcStages) & 1));   // landed
+        const int s_ = step % STAGES;
+        mbar_wait_bounded(smem_addr(kv_full + s_), static_cast<uint32_t>((step / STAGES) & 1));   // landed
         const int z0 = max(0, len - kbase);
-        unsigned char* vst = smem + Sh::RING_OFF + s * Sh::STAGE_BYTES + Sh::K_BYTES;
-        for (int i = tid; i < (kTcKeys - z0) * 8 * DH; i += 128) {
-          const int dh = i / ((kTcKeys - z0) * 8), rem = i % ((kTcKeys - z0) * 8);
+        unsigned char* vst = smem + Sh::RING_OFF + s_ * Sh::STAGE_BYTES + Sh::K_BYTES;
+        for (int q = r; q < (kTcKeys - z0) * 8 * DH; q += 128) {
+          const int dh = q / ((kTcKeys - z0) * 8), rem = q % ((kTcKeys - z0) * 8);
           *reinterpret_cast<uint4*>(vst + dh * Sh::KV_REGION + (z0 + rem / 8) * 128 + (rem % 8) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
@@ -487,18 +567,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
       fence_proxy_async_smem();   // generic-proxy writes of P (and V zeros) before the MMA reads them
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(p_full));
+      if (lane == 0) mbar_arrive(smem_addr(tb + 4));
     }
     // ---- epilogue: O / l for the real rows
-    if (ok && !*abort_flag) {
-      if (mbar_wait_bounded(smem_addr(pv_done), static_cast<uint32_t>((n_tiles - 1) & 1))) {
+    if (active && ok && !*abort_flag) {
+      if (mbar_wait_bounded(smem_addr(tb + 5), static_cast<uint32_t>((t_cnt - 1) & 1))) {
         tc_fence_after();
         const float inv = 1.f / l;
         float* dst = a.out + ((static_cast<int64_t>(q0) + tok) * a.Hq + h * G + (r % G)) * D;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float o[32];
-          tmem_ld32(tmem + lane_addr + c, o);
+          tmem_ld32(tm + c, o);
           if (row_real) {
 #pragma unroll
             for (int k = 0; k < 32; k += 4)
@@ -513,7 +593,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) paged_prefill_tc_kernel(const _
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == Sh::MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, Sh::TMEM_COLS);
   }

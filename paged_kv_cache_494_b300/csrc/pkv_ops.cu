@@ -147,6 +147,25 @@ KernelPair pick_g(int dtype, int g, bool simt) {
   }
 }
 
+// tcgen05 prefill kernels: two Q tiles per CTA (one CTA per SM) sharing a 2-stage ring of 64-key steps.
+constexpr int kTcTiles = 2, kTcStages = 2;
+struct TcKernel {
+  void (*kern)(pkv_dev::PrefillArgs, pkv_dev::TcMaps) = nullptr;
+  size_t smem = 0;
+  int item = 0;      // query tokens per CTA
+  int threads = 0;
+};
+template <int D, int G, int NT, int ST>
+TcKernel tc_pick(int32_t n_seqs) {
+  using Sh = pkv_dev::TcShape<D, G, NT, ST>;
+  TcKernel k;
+  k.kern = pkv_dev::paged_prefill_tc_kernel<D, G, NT, ST>;
+  k.smem = pkv_dev::prefill_tc_smem_bytes<Sh>(n_seqs);
+  k.item = NT * Sh::TQ;
+  k.threads = Sh::THREADS;
+  return k;
+}
+
 // Prefill runs on the tcgen05 kernel unless PKV_PREFILL_PATH=mma (the mma.sync kernel, kept to
 // cross-check the two) or the batch has more sequences than the tcgen05 kernel keeps in shared memory.
 constexpr int32_t kPrefillTcMaxSeqs = 2048;
@@ -162,6 +181,8 @@ bool force_simt() {
 }
 
 KernelPair pick_fp8(int g) {
+  // PKV_DECODE_FP8_CTAS=4: the G = 4 fp8 kernel compiled for 4 resident CTAs per SM (128 registers)
+  if (g == 4 && env_int("PKV_DECODE_FP8_CTAS", 3) == 4) return pair_for<pkv_dev::Fp8Math<4, 4>, 128, 4>(MAPS_FP8);
   switch (g) {
     case 1: return pair_for<pkv_dev::Fp8Math<1>, 128, 1>(MAPS_FP8);
     case 2: return pair_for<pkv_dev::Fp8Math<2>, 128, 2>(MAPS_FP8);
@@ -470,25 +491,24 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   a.MB = d.max_blocks_per_seq;
   a.window = window;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.stages = pkv_dev::kTcStages;
+  a.stages = 0;   // the tcgen05 kernel fixes its ring depth at compile time
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (prefill_path_tc() && n_seqs <= kPrefillTcMaxSeqs) {
     // tensor-core path: tcgen05.mma with accumulators in tensor memory, 128-row tiles
-    using TK = void (*)(pkv_dev::PrefillArgs, pkv_dev::TcMaps);
-    TK kern = nullptr;
-    size_t smem = 0;
-    int tq = 0;
-#define PKV_TC_CASE(DD, GG)                                            \
-    if (d.head_dim == DD && g == GG) {                                 \
-      kern = pkv_dev::paged_prefill_tc_kernel<DD, GG>;                 \
-      smem = pkv_dev::prefill_tc_smem_bytes<DD, GG>(n_seqs);           \
-      tq = pkv_dev::TcShape<DD, GG>::TQ;                               \
-    }
+    TcKernel tk;
+    const int variant = env_int("PKV_PREFILL_TC_VARIANT", 0);   // 0: default ring depth / P buffers
+#define PKV_TC_CASE(DD, GG)        \
+    if (d.head_dim == DD && g == GG) tk = tc_pick<DD, GG, kTcTiles, kTcStages>(n_seqs);
     PKV_TC_CASE(64, 1) PKV_TC_CASE(64, 2) PKV_TC_CASE(64, 3) PKV_TC_CASE(64, 4)
     PKV_TC_CASE(64, 5) PKV_TC_CASE(64, 6) PKV_TC_CASE(64, 7) PKV_TC_CASE(64, 8)
     PKV_TC_CASE(128, 1) PKV_TC_CASE(128, 2) PKV_TC_CASE(128, 3) PKV_TC_CASE(128, 4)
     PKV_TC_CASE(128, 5) PKV_TC_CASE(128, 6) PKV_TC_CASE(128, 7) PKV_TC_CASE(128, 8)
 #undef PKV_TC_CASE
+    if (d.head_dim == 128 && g == 4 && variant == 1) tk = tc_pick<128, 4, 1, 3>(n_seqs);
+    if (d.head_dim == 128 && g == 4 && variant == 2 && n_seqs <= 256) tk = tc_pick<128, 4, 2, 3>(n_seqs);
+    auto kern = tk.kern;
+    const size_t smem = tk.smem;
+    const int tq = tk.item;
     if (!kern) return PKV_ERR_INVALID;
     if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return PKV_ERR_CUDA;
     pkv_dev::TcMaps maps;
@@ -498,7 +518,7 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
       return PKV_ERR_CUDA;
     const int64_t tiles_ub = (static_cast<int64_t>(total_q) + tq - 1) / tq + n_seqs;   // >= sum of tiles
     if (tiles_ub > 0x7fffffffLL) return PKV_ERR_INVALID;
-    if (launch(kern, dim3(static_cast<unsigned>(tiles_ub), d.num_kv_heads), dim3(pkv_dev::kTcThreads), smem, st, a,
+    if (launch(kern, dim3(static_cast<unsigned>(tiles_ub), d.num_kv_heads), dim3(tk.threads), smem, st, a,
                maps) != cudaSuccess ||
         cudaGetLastError() != cudaSuccess)
       return PKV_ERR_CUDA;
