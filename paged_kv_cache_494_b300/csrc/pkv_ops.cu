@@ -147,8 +147,8 @@ KernelPair pick_g(int dtype, int g, bool simt) {
   }
 }
 
-// tcgen05 prefill kernels: two Q tiles per CTA (one CTA per SM) sharing a 2-stage ring of 64-key steps.
-constexpr int kTcTiles = 2, kTcStages = 2;
+// tcgen05 prefill kernels: two Q tiles per CTA (one CTA per SM) sharing a 4-stage ring of 64-key steps.
+constexpr int kTcTiles = 2, kTcStages = 4;
 struct TcKernel {
   void (*kern)(pkv_dev::PrefillArgs, pkv_dev::TcMaps) = nullptr;
   size_t smem = 0;
@@ -494,9 +494,8 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   a.stages = 0;   // the tcgen05 kernel fixes its ring depth at compile time
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (prefill_path_tc() && n_seqs <= kPrefillTcMaxSeqs) {
-    // tensor-core path: tcgen05.mma with accumulators in tensor memory, 128-row tiles
+    // tensor-core path: tcgen05.mma with S, P and O in tensor memory, two 128-row Q tiles per work item
     TcKernel tk;
-    const int variant = env_int("PKV_PREFILL_TC_VARIANT", 0);   // 0: default ring depth / P buffers
 #define PKV_TC_CASE(DD, GG)        \
     if (d.head_dim == DD && g == GG) tk = tc_pick<DD, GG, kTcTiles, kTcStages>(n_seqs);
     PKV_TC_CASE(64, 1) PKV_TC_CASE(64, 2) PKV_TC_CASE(64, 3) PKV_TC_CASE(64, 4)
@@ -504,8 +503,6 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
     PKV_TC_CASE(128, 1) PKV_TC_CASE(128, 2) PKV_TC_CASE(128, 3) PKV_TC_CASE(128, 4)
     PKV_TC_CASE(128, 5) PKV_TC_CASE(128, 6) PKV_TC_CASE(128, 7) PKV_TC_CASE(128, 8)
 #undef PKV_TC_CASE
-    if (d.head_dim == 128 && g == 4 && variant == 1) tk = tc_pick<128, 4, 1, 3>(n_seqs);
-    if (d.head_dim == 128 && g == 4 && variant == 2 && n_seqs <= 256) tk = tc_pick<128, 4, 2, 3>(n_seqs);
     auto kern = tk.kern;
     const size_t smem = tk.smem;
     const int tq = tk.item;
@@ -516,10 +513,12 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
     if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d) ||
         !encode_q_map(&maps.q, q, total_q, num_q_heads, d.head_dim, g))
       return PKV_ERR_CUDA;
-    const int64_t tiles_ub = (static_cast<int64_t>(total_q) + tq - 1) / tq + n_seqs;   // >= sum of tiles
-    if (tiles_ub > 0x7fffffffLL) return PKV_ERR_INVALID;
-    if (launch(kern, dim3(static_cast<unsigned>(tiles_ub), d.num_kv_heads), dim3(tk.threads), smem, st, a,
-               maps) != cudaSuccess ||
+    // persistent: one CTA per SM (or fewer when there are fewer work items)
+    const int64_t items_ub = ((static_cast<int64_t>(total_q) + tq - 1) / tq + n_seqs) * d.num_kv_heads;
+    const int sms = num_sms();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    const unsigned grid = static_cast<unsigned>(items_ub < sms ? items_ub : sms);
+    if (launch(kern, dim3(grid), dim3(tk.threads), smem, st, a, maps) != cudaSuccess ||
         cudaGetLastError() != cudaSuccess)
       return PKV_ERR_CUDA;
     return PKV_OK;
