@@ -339,8 +339,25 @@ PKV_API pkv_status pkv_paged_decode_static(const pkv_pool* pool, float* out, con
 
 /* Synchronise the current device, then return and clear the error recorded by kernels
  * (PKV_ERR_DEVICE_BOUNDS / PKV_ERR_DEVICE_TIMEOUT), PKV_ERR_CUDA if the device reports an error,
- * else PKV_OK. pool may be NULL. */
+ * else PKV_OK. Reads the process-wide error word and, when pool is not NULL and has one, the pool's
+ * own word (pkv_pool_set_error_word). pool may be NULL. */
 PKV_API pkv_status pkv_last_error(const pkv_pool* pool);
+
+/* Per-pool error reporting (no counterpart on the pages: it serves this library's failure
+ * detection). By default every kernel records a bad block id or slot (PKV_ERR_DEVICE_BOUNDS) or a
+ * bounded wait that gave up (PKV_ERR_DEVICE_TIMEOUT) in one process-wide word, which only
+ * pkv_last_error reads, after synchronising the whole device. A caller that serves several streams
+ * or pools gives each pool its own word instead: d_word is a device pointer to one uint32_t owned
+ * by the caller (4-byte aligned, zeroed by the caller before first use; NULL returns the pool to
+ * the process-wide word). From then on the pool's device operations record into d_word with
+ * atomicOr. The library allocates nothing. Calls that overlap on the GPU share the word. */
+PKV_API pkv_status pkv_pool_set_error_word(pkv_pool* pool, uint32_t* d_word);
+
+/* Reads and clears the pool's error word in stream order on `stream`, then waits for that stream
+ * only (no device-wide synchronisation): PKV_ERR_DEVICE_BOUNDS / PKV_ERR_DEVICE_TIMEOUT if a kernel
+ * of this pool recorded one before this point of the stream, PKV_ERR_CUDA if a CUDA call failed,
+ * PKV_ERR_INVALID if the pool has no error word, else PKV_OK. */
+PKV_API pkv_status pkv_stream_error(const pkv_pool* pool, void* stream);
 
 /* ---- diagnostics -------------------------------------------------------------------------- */
 /* Self-test of the bounded waits of the pipelined kernels (no counterpart on the pages: it checks

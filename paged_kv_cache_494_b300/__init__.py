@@ -86,6 +86,8 @@ _SIGS = {
     "pkv_paged_decode_static": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _i32,
                                                _vp]),
     "pkv_last_error": (ctypes.c_int, [_vp]),
+    "pkv_pool_set_error_word": (ctypes.c_int, [_vp, _vp]),
+    "pkv_stream_error": (ctypes.c_int, [_vp, _vp]),
     "pkv_selftest_wait_timeout": (ctypes.c_int, [_vp, _vp]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
@@ -381,3 +383,13 @@ class Pool:
 
     def last_error(self) -> int:
         return lib.pkv_last_error(self._h)
+
+    def set_error_word(self, word) -> None:
+        """pkv_pool_set_error_word: the pool's kernels record errors into `word` (a one-element
+        device int32 / uint32 tensor the caller zeroes), or the process-wide word again for None."""
+        _check(lib.pkv_pool_set_error_word(self._h, _dev(word)), "pkv_pool_set_error_word")
+
+    def stream_error(self, stream=None) -> int:
+        """pkv_stream_error: read and clear the pool's error word in stream order; waits for that
+        stream only."""
+        return lib.pkv_stream_error(self._h, _stream(stream))

@@ -19,7 +19,8 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
                                                                 const int64_t* __restrict__ slots, int32_t n_tokens,
                                                                 int32_t Hkv, int32_t PPR, int32_t B, int64_t n_slots,
                                                                 uint4* __restrict__ k_cache,
-                                                                uint4* __restrict__ v_cache) {
+                                                                uint4* __restrict__ v_cache, unsigned int* err) {
+  set_error_word(err);
   pdl_wait();
   pdl_launch_dependents();
   const int64_t total = static_cast<int64_t>(n_tokens) * Hkv * PPR;
@@ -52,7 +53,9 @@ struct LayerCaches {
 
 // grid.x = n_pairs * num_layers; each CTA copies one K block and one V block (PPB pieces each).
 __global__ void __launch_bounds__(256) copy_blocks_kernel(LayerCaches caches, const int32_t* __restrict__ pairs,
-                                                          int32_t num_layers, int64_t PPB, int32_t num_blocks) {
+                                                          int32_t num_layers, int64_t PPB, int32_t num_blocks,
+                                                          unsigned int* err) {
+  set_error_word(err);
   pdl_wait();
   pdl_launch_dependents();
   const int32_t pair = blockIdx.x / num_layers;
@@ -109,7 +112,8 @@ template <int D>
 __global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, const int64_t* __restrict__ slots,
     int32_t n_tokens, int32_t Hkv, int32_t B, int64_t n_slots, uint8_t* __restrict__ k8, uint8_t* __restrict__ v8t,
-    float* __restrict__ ks, float* __restrict__ vs) {
+    float* __restrict__ ks, float* __restrict__ vs, unsigned int* err) {
+  set_error_word(err);
   pdl_wait();
   pdl_launch_dependents();
   constexpr int E = D / 32;

@@ -69,6 +69,7 @@ struct DecodeArgs {
   const float* k_scale;          // fp8 pools: [NB][Hkv][B] per-(token, head) scales (else unused)
   const float* v_scale;
   unsigned long long tag;        // 48-bit tag of this call for ws_count
+  unsigned int* err;             // error word of the call's pool (null: the process-wide word)
 };
 
 // Arrival of one segment of a split unit. Returns true for the warp that completes the unit.
@@ -978,6 +979,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   // not used by the prefix build; the barrier after it orders the zeroing before any arrival.
   int32_t* cta_cnt = wsum + 16;
   if (threadIdx.x < NW) cta_cnt[threadIdx.x] = 0;
+  set_error_word(a.err);
   pdl_wait();
   build_prefix(a, pref, ipref, cfirst, wsum);
   if (lane == 0) {

@@ -29,6 +29,7 @@ struct PrefillArgs {
   const int32_t* cu_q;           // [n_seqs + 1] query rows of sequence b: cu_q[b] .. cu_q[b+1]
   int32_t n_seqs, Hq, Hkv, B, NB, MB, window, stages;
   float scale_log2;
+  unsigned int* err;             // error word of the call's pool (null: the process-wide word)
 };
 
 template <int D, int G>
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(128, 4) paged_prefill_kernel(const __grid_cons
   int32_t* tpref = wsum + 64;          // [n + 1] query-tile prefix over sequences
   int32_t* tab = tpref + (n + 1);      // block-table entries of this CTA's chunk range
 
+  set_error_word(a.err);
   pdl_wait();
 
   // ---- query-tile prefix over sequences (block-wide scan)

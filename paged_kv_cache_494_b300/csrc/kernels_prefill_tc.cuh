@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
   int32_t* wsum = reinterpret_cast<int32_t*>(smem + Sh::MISC_OFF + 16);
   int32_t* tpref = wsum + 64;
 
+  set_error_word(a.err);
   pdl_wait();   // before any global access, and before holding tensor memory
 
   // ---- items per sequence (prefix over sequences) and the largest count

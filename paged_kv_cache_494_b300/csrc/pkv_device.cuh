@@ -13,10 +13,22 @@ namespace pkv_dev {
 // Error bits recorded by kernels, read and cleared by pkv_last_error.
 enum : unsigned int { ERRBIT_BOUNDS = 1u, ERRBIT_TIMEOUT = 2u };
 
-// Kernel error word. This header is included by exactly one translation unit (pkv_ops.cu).
+// Kernel error word of the process. This header is included by exactly one translation unit
+// (pkv_ops.cu).
 __device__ unsigned int g_error_bits = 0;
 
-__device__ __forceinline__ void record_error(unsigned int bit) { atomicOr(&g_error_bits, bit); }
+// Error word of the running kernel: the word of the pool the call belongs to (set with
+// pkv_pool_set_error_word), or null for the process-wide word. Every kernel stores it here first
+// thing (all threads store the same value), so code deep inside a kernel (bounded waits included)
+// records into the right word without carrying the pointer.
+__shared__ unsigned int* s_err_word;
+
+__device__ __forceinline__ void set_error_word(unsigned int* w) { s_err_word = w; }
+
+__device__ __forceinline__ void record_error(unsigned int bit) {
+  unsigned int* w = s_err_word;
+  atomicOr(w ? w : &g_error_bits, bit);
+}
 
 // Upper bound on mbarrier polls before a wait gives up. Each try_wait may itself suspend the thread
 // for a hardware-chosen interval (measured on B300: ~4 us per unsatisfied poll), so a stuck wait

@@ -29,6 +29,7 @@ namespace pkv_dev {
 // No copy or other asynchronous operation is in flight, so the block can exit at once.
 __global__ void selftest_wait_kernel(int32_t* gave_up) {
   __shared__ __align__(8) uint64_t bar;
+  set_error_word(nullptr);
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&bar), 1);
     fence_mbar_init();
@@ -367,6 +368,7 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   pl.k = pick_kernels(d.dtype, d.head_dim, g);
   if (!pl.k.decode) return PKV_ERR_INVALID;
   pl.nw = env_int("PKV_DECODE_WARPS", 4);
+  if (pl.nw > 4) pl.nw = 4;   // the decode kernels are compiled for at most 128 threads per CTA
   pl.stages = env_int("PKV_DECODE_STAGES", 2);
   pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.stage_bytes, n_seqs, partition_tokens > 0, window > 0);
   // every CTA keeps per-sequence prefix sums in shared memory: the batch must fit beside the ring
@@ -427,7 +429,7 @@ pkv_status pkv_reshape_and_cache(const pkv_pool* p, const void* k, const void* v
                                static_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
                                static_cast<const uint4*>(v), slots, n_tokens, d.num_kv_heads, ppr, d.block_size,
                                static_cast<int64_t>(d.num_blocks) * d.block_size, static_cast<uint4*>(k_cache),
-                               static_cast<uint4*>(v_cache));
+                               static_cast<uint4*>(v_cache), p->d_err_word);
   return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -453,7 +455,7 @@ pkv_status pkv_copy_blocks(const pkv_pool* p, void* const* k_caches, void* const
   if (grid > 0x7fffffff) return PKV_ERR_INVALID;
   const cudaError_t e = launch(pkv_dev::copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
                                static_cast<cudaStream_t>(stream), lc, pairs, d.num_layers, block_bytes / 16,
-                               d.num_blocks);
+                               d.num_blocks, p->d_err_word);
   return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -491,6 +493,7 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   a.MB = d.max_blocks_per_seq;
   a.window = window;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = p->d_err_word;
   a.stages = 0;   // the tcgen05 kernel fixes its ring depth at compile time
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (prefill_path_tc() && n_seqs <= kPrefillTcMaxSeqs) {
@@ -610,7 +613,7 @@ pkv_status pkv_reshape_and_cache_fp8(const pkv_pool* p, const void* k, const voi
                                static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slots,
                                n_tokens, d.num_kv_heads, d.block_size,
                                static_cast<int64_t>(d.num_blocks) * d.block_size, static_cast<uint8_t*>(k_cache),
-                               static_cast<uint8_t*>(v_cache), k_scale, v_scale);
+                               static_cast<uint8_t*>(v_cache), k_scale, v_scale, p->d_err_word);
   return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -642,9 +645,9 @@ pkv_status pkv_copy_blocks_fp8(const pkv_pool* p, void* const* k_caches, void* c
   if (grid > 0x7fffffff) return PKV_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch(pkv_dev::copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, codes, pairs,
-             d.num_layers, code_bytes / 16, d.num_blocks) != cudaSuccess ||
+             d.num_layers, code_bytes / 16, d.num_blocks, p->d_err_word) != cudaSuccess ||
       launch(pkv_dev::copy_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, scales, pairs,
-             d.num_layers, scale_bytes / 16, d.num_blocks) != cudaSuccess ||
+             d.num_layers, scale_bytes / 16, d.num_blocks, p->d_err_word) != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
@@ -715,6 +718,7 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   // 16 chunks per warp are unaffected).
   a.min_chunks = env_int("PKV_DECODE_MIN_CHUNKS", 16);
   a.tag = next_call_tag();
+  a.err = p->d_err_word;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
@@ -731,15 +735,43 @@ pkv_status pkv_selftest_wait_timeout(int32_t* gave_up, void* stream) {
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status pkv_last_error(const pkv_pool*) {
+static pkv_status error_status(unsigned int bits) {
+  if (bits & pkv_dev::ERRBIT_TIMEOUT) return PKV_ERR_DEVICE_TIMEOUT;
+  if (bits & pkv_dev::ERRBIT_BOUNDS) return PKV_ERR_DEVICE_BOUNDS;
+  return PKV_OK;
+}
+
+pkv_status pkv_last_error(const pkv_pool* p) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
   unsigned int bits = 0;
   if (cudaMemcpyFromSymbol(&bits, pkv_dev::g_error_bits, sizeof bits) != cudaSuccess) return PKV_ERR_CUDA;
   const unsigned int zero = 0;
   if (bits && cudaMemcpyToSymbol(pkv_dev::g_error_bits, &zero, sizeof zero) != cudaSuccess) return PKV_ERR_CUDA;
-  if (bits & pkv_dev::ERRBIT_TIMEOUT) return PKV_ERR_DEVICE_TIMEOUT;
-  if (bits & pkv_dev::ERRBIT_BOUNDS) return PKV_ERR_DEVICE_BOUNDS;
+  if (p && p->d_err_word) {   // the pool's own word as well
+    unsigned int pb = 0;
+    if (cudaMemcpy(&pb, p->d_err_word, sizeof pb, cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+    if (pb && cudaMemset(p->d_err_word, 0, sizeof pb) != cudaSuccess) return PKV_ERR_CUDA;
+    bits |= pb;
+  }
+  return error_status(bits);
+}
+
+pkv_status pkv_pool_set_error_word(pkv_pool* p, uint32_t* d_word) {
+  if (!p) return PKV_ERR_INVALID;
+  if (d_word && (reinterpret_cast<uintptr_t>(d_word) & 3u)) return PKV_ERR_INVALID;
+  p->d_err_word = reinterpret_cast<unsigned int*>(d_word);
   return PKV_OK;
+}
+
+pkv_status pkv_stream_error(const pkv_pool* p, void* stream) {
+  if (!p || !p->d_err_word) return PKV_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int bits = 0;
+  // on the stream: read the word, then clear it; only this stream is waited for
+  if (cudaMemcpyAsync(&bits, p->d_err_word, sizeof bits, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(p->d_err_word, 0, sizeof bits, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return error_status(bits);
 }
 
 }  // extern "C"

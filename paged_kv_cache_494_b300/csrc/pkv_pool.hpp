@@ -58,6 +58,8 @@ struct pkv_pool {
   int64_t next_entry_id = 0;
   std::list<int32_t> evictable;               // cached blocks held only by the cache, oldest first
   std::unordered_map<int32_t, std::list<int32_t>::iterator> evictable_pos;
+  // device error word the pool's kernels record into (pkv_pool_set_error_word); null: process-wide
+  unsigned int* d_err_word = nullptr;
 };
 
 namespace pkv {
