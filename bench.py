@@ -755,18 +755,18 @@ def decode_pool(pkv, name: str, seed: int, fp8: bool, full_pool: bool):
                         initial_free_list=synth.free_list(NB, seed))
         seqs = [pool.alloc(-1, int(t))[0] for t in lens]
     tables, l = pool.block_table(seqs)
-    return w, pool, NB, tables, l
+    return w, pool, NB, tables, l, seqs
 
 
 class DecodeProblem:
     """One layer of a decode workload on the device: pool, caches, q, tables, output, workspace."""
 
     def __init__(self, name: str, seed: int, fp8: bool = False, full_pool: bool = True,
-                 partition_tokens=None):
+                 partition_tokens=None, cascade: bool = False):
         import torch
         import paged_kv_cache_494_b300 as pkv
         self.torch, self.pkv, self.fp8 = torch, pkv, fp8
-        w, pool, NB, tables, l = decode_pool(pkv, name, seed, fp8, full_pool)
+        w, pool, NB, tables, l, seqs = decode_pool(pkv, name, seed, fp8, full_pool)
         self.w, self.pool, self.NB = w, pool, NB
         g = torch.Generator(device="cuda").manual_seed(seed)
         if fp8:
@@ -785,14 +785,26 @@ class DecodeProblem:
         self.q = torch.randn(self.n, w.num_q_heads, w.head_dim, device="cuda", dtype=qdt, generator=g)
         self.out = torch.empty(self.n, w.num_q_heads, w.head_dim, device="cuda")
         self.pt = w.partition_tokens if partition_tokens is None else partition_tokens
-        self.ws = torch.empty(pool.decode_workspace_bytes(self.n, w.num_q_heads, self.pt) // 4 + 4, device="cuda")
+        # cascade: the blocks every sequence shares (the allocator's sharing structure) are attended
+        # once for the batch, then merged with each sequence's private suffix
+        self.cascade = cascade
+        self.prefix_blocks = pool.shared_prefix_blocks(seqs) if cascade else 0
+        wsb = (pool.shared_prefix_workspace_bytes(self.n, w.num_q_heads, self.prefix_blocks) if cascade
+               else pool.decode_workspace_bytes(self.n, w.num_q_heads, self.pt))
+        self.ws = torch.empty(wsb // 4 + 4, device="cuda")
         self.tab, self.lens = torch.from_numpy(tables).cuda(), torch.from_numpy(l).cuda()
         self.lens_host = l
         per = (w.head_dim + 4) * 2 if fp8 else w.head_dim * 2 * w.elem_bytes
         self.kv_bytes = int(l.sum()) * w.num_kv_heads * per      # logical KV bytes one launch reads
+        # distinct KV bytes: every physical block a launch touches, counted once
+        self.unique_bytes = len({int(b) for row, n_ in zip(tables, l) for b in row[:-(-int(n_) // w.block_size)]}) \
+            * w.block_size * w.num_kv_heads * per
 
     def run(self):
-        if self.fp8:
+        if self.cascade:
+            self.pool.paged_decode_shared_prefix(self.out, self.q, self.kc, self.vc, self.tab, self.lens, self.w.scale,
+                                                 self.prefix_blocks, self.ws)
+        elif self.fp8:
             self.pool.paged_decode_fp8(self.out, self.q, self.kc, self.vc, self.ksc, self.vsc, self.tab, self.lens,
                                        self.w.scale, 0, self.pt, self.ws)
         else:
@@ -800,14 +812,15 @@ class DecodeProblem:
                                    self.ws)
 
 
-def decode_entry(name: str, seed: int, peak: float, flush, partition_tokens=None, n_iter: int = 20):
+def decode_entry(name: str, seed: int, peak: float, flush, partition_tokens=None, n_iter: int = 20,
+                 cascade: bool = False):
     """One decode workload: median of n_iter launches with L2 flushed before each (the number
     reported for every workload), and the average of n_iter launches back to back. GB/s and the
-    roofline fraction use the logical KV bytes a launch reads; where the committed ncu record of the
-    same kernel code has the launch's DRAM bytes, they are reported too (and the fraction on DRAM
-    bytes for the shared-prefix workload, whose shared pages are served from L2)."""
+    roofline fraction use the logical KV bytes a launch reads (for the shared-prefix workload: the
+    distinct blocks, each once); where the committed ncu record of the same kernel code has the
+    launch's DRAM bytes, they are reported too. cascade=True runs the shared-prefix entry point."""
     import torch
-    p = DecodeProblem(name, seed, partition_tokens=partition_tokens)
+    p = DecodeProblem(name, seed, partition_tokens=partition_tokens, cascade=cascade)
     for _ in range(3):
         p.run()
     torch.cuda.synchronize()
@@ -826,18 +839,23 @@ def decode_entry(name: str, seed: int, peak: float, flush, partition_tokens=None
          "b2b_us_per_launch": round(1e3 * tb, 2), "b2b_gb_per_s": round(p.kv_bytes / (tb * 1e-3) / 1e9, 1),
          "timing": f"median of {n_iter} launches (one-launch CUDA graph replays), L2 flushed before each; "
                    f"b2b = mean of {n_iter} launches back to back in one CUDA graph (no flush)"}
+    if p.w.length_kind == "prefix":
+        # the children's shared prompt blocks are one set of physical pages: the bytes a launch must
+        # bring from memory count each distinct block once
+        ach = p.unique_bytes / (t * 1e-3) / 1e9
+        e["unique_kv_bytes_per_launch"] = p.unique_bytes
+        e["roofline"].update(achieved=round(ach, 1), frac=round(ach / peak, 4), achieved_logical=round(gbs, 1),
+                             basis="distinct physical KV blocks a launch reads, each counted once")
+    if cascade:
+        e["method"] = ("cascade: blocks shared by every sequence attended once for the batch on tensor cores, "
+                       "private suffixes by the decode kernel, log-sum-exp merge")
+        e["prefix_blocks"] = p.prefix_blocks
     key = name if (partition_tokens is None or partition_tokens == p.w.partition_tokens) else None
+    if key is not None and cascade:
+        key += "_cascade"
     rec = decode_traffic_record(key) if key else None
     if rec is not None:
-        dram = int(rec["bytes_per_launch_profile"] * p.kv_bytes / rec["algorithmic_bytes_profile"])
-        e["dram_bytes_per_launch"] = dram
-        if p.w.length_kind == "prefix":
-            e["roofline"]["achieved_logical"] = e["roofline"]["achieved"]
-            e["roofline"]["achieved"] = round(dram / (t * 1e-3) / 1e9, 1)
-            e["roofline"]["frac"] = round(dram / (t * 1e-3) / 1e9 / peak, 4)
-            e["roofline"]["basis"] = "ncu DRAM bytes per launch (shared prompt pages are read from L2)"
-    elif p.w.length_kind == "prefix":
-        e["roofline"]["basis"] = "logical bytes (no ncu DRAM record for this kernel code)"
+        e["dram_bytes_per_launch"] = int(rec["bytes_per_launch_profile"] * p.kv_bytes / rec["algorithmic_bytes_profile"])
     del p
     torch.cuda.empty_cache()
     return e
@@ -898,6 +916,7 @@ def bench_workloads(args, local: int):
         out["tiny_f32"] = decode_entry("tiny_f32", args.seed, peak, flush)
         out["gqa5_bf16"] = decode_entry("gqa5_bf16", args.seed, peak, flush)
         out["prefix_cow_bf16"] = decode_entry("prefix_cow_bf16", args.seed, peak, flush)
+        out["prefix_cow_bf16_cascade"] = decode_entry("prefix_cow_bf16", args.seed, peak, flush, cascade=True)
         out["long_split_bf16"] = decode_entry("long_split_bf16", args.seed, peak, flush)
         out["long_split_bf16_balanced"] = decode_entry("long_split_bf16", args.seed, peak, flush, partition_tokens=0)
         out["serve256_fp8"] = fp8_step_entry(args, peak, local)
@@ -913,13 +932,13 @@ def profile_decode(args):
     (8 x 32,768 tokens, 512-token partitions as the workload states; pool cut to twice its pages)."""
     fp8 = args.workload == "serve256_fp8"
     name = WORKLOAD if fp8 else args.workload
-    p = DecodeProblem(name, args.seed, fp8=fp8, full_pool=False)
+    p = DecodeProblem(name, args.seed, fp8=fp8, full_pool=False, cascade=args.cascade)
     for _ in range(5):
         p.run()
     p.torch.cuda.synchronize()
     assert p.pkv.last_error() == p.pkv.OK
     print(json.dumps({"profile_decode": args.workload, "layers": 1, "kv_bytes_per_launch": p.kv_bytes, "NB": p.NB,
-                      "partition_tokens": p.pt}))
+                      "partition_tokens": p.pt, "cascade": args.cascade}))
 
 
 def main(argv=None):
@@ -938,6 +957,8 @@ def main(argv=None):
                                            "long_split_bf16", "gqa5_bf16", "tiny_f32"], default=WORKLOAD,
                     help="serve256_bf16 (the benchmark line), serve256_fp8 (the same step on an fp8 pool) or "
                          "prefill_bf16 (causal prefill kernel line)")
+    ap.add_argument("--cascade", action="store_true",
+                    help="with --profile-decode --workload prefix_cow_bf16: the shared-prefix entry point")
     ap.add_argument("--profile-decode", action="store_true",
                     help="run one layer's decode 5 times (small case for ncu); prints no bench line")
     args = ap.parse_args(argv)

@@ -192,6 +192,13 @@ PKV_API pkv_status pkv_prefix_evict(pkv_pool* pool, int32_t max_blocks, int32_t*
 /* Number of cached blocks and of evictable ones (either output may be NULL). */
 PKV_API pkv_status pkv_prefix_stats(const pkv_pool* pool, int32_t* n_cached_blocks, int32_t* n_evictable);
 
+/* Sharing structure for pkv_paged_decode_shared_prefix: *out_blocks = the number of leading logical
+ * blocks k that every one of the n live sequences maps to the same physical block (a prompt forked
+ * into children, whose full blocks stay shared until copy-on-write), counting only blocks that are
+ * full in every sequence (k < len / block_size for the shortest one). n >= 1. */
+PKV_API pkv_status pkv_shared_prefix_blocks(const pkv_pool* pool, const int32_t* seqs, int32_t n,
+                                            int32_t* out_blocks);
+
 /* Host copies of the block tables of n live sequences: table_out[n][max_blocks_per_seq]
  * (int32, unused entries -1) and lens_out[n]. Either output may be NULL. */
 PKV_API pkv_status pkv_block_table(const pkv_pool* pool, const int32_t* seqs, int32_t n, int32_t* table_out,
@@ -305,6 +312,37 @@ PKV_API pkv_status pkv_paged_prefill(const pkv_pool* pool, float* out, const voi
                                      const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
                                      const int32_t* cu_q, int32_t n_seqs, int32_t total_q, int32_t num_q_heads,
                                      float scale, int32_t window, void* stream);
+
+/* Shared-prefix (cascade) decode: pkv_paged_decode's result for a batch whose sequences all begin with
+ * the same prefix_blocks physical blocks (a forked prompt whose children share its full blocks by
+ * reference count until one of them writes: "Paged Attention optimiza el uso de memoria en LLMs",
+ * copy-on-write paragraph; "PagedAttention e vLLM", "Implementazione nel mondo reale").
+ * The shared blocks are read once for the whole batch instead of once per sequence: every query row
+ * of the batch attends to them in one tensor-core pass (the rows of all sequences stacked as the M
+ * side of each matrix product, split over the keys to fill the GPU), each sequence's private suffix
+ * t in [prefix_blocks * B, len_b) is attended by the decode kernel, and the two parts are combined by
+ * their log-sum-exp ("Servicio de modelos de lenguaje con un presupuesto de memoria" §6), so `out`
+ * is the exact attention over [0, len_b) to rounding.
+ * Arguments as pkv_paged_decode (partition_tokens fixed to 0), plus prefix_blocks: how many leading
+ * table entries every sequence shares. Requires block_tables[b][k] == block_tables[0][k] for every
+ * b < n_seqs and k < prefix_blocks (a mismatch is recorded as PKV_ERR_DEVICE_BOUNDS, and the rows
+ * are then attended over sequence 0's prefix) and context_lens[b] >= prefix_blocks * B (a shorter
+ * sequence records PKV_ERR_DEVICE_BOUNDS). prefix_blocks = 0 is pkv_paged_decode.
+ * Needs a bf16 pool with D 64 or 128, block size a multiple of 16 and num_q_heads / Hkv <= 8;
+ * otherwise PKV_ERR_INVALID. workspace: at least pkv_decode_shared_prefix_workspace_bytes(...)
+ * bytes, no initialisation needed; concurrent calls must not share one. Launches three kernels on
+ * `stream`. */
+PKV_API pkv_status pkv_paged_decode_shared_prefix(const pkv_pool* pool, float* out, const void* q,
+                                                  const void* k_cache, const void* v_cache,
+                                                  const int32_t* block_tables, const int32_t* context_lens,
+                                                  int32_t n_seqs, int32_t num_q_heads, float scale,
+                                                  int32_t prefix_blocks, void* workspace, size_t workspace_bytes,
+                                                  void* stream);
+
+/* Workspace bytes pkv_paged_decode_shared_prefix needs (prefix_blocks = 0: those of pkv_paged_decode
+ * without partitions; 0 for unsupported arguments). */
+PKV_API size_t pkv_decode_shared_prefix_workspace_bytes(const pkv_pool* pool, int32_t n_seqs, int32_t num_q_heads,
+                                                        int32_t prefix_blocks);
 
 /* Workspace bytes pkv_paged_decode needs for these arguments on the current device. */
 PKV_API size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t n_seqs, int32_t num_q_heads,

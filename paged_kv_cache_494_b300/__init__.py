@@ -68,6 +68,7 @@ _SIGS = {
     "pkv_prefix_evict": (ctypes.c_int, [_vp, _i32, _pi32]),
     "pkv_prefix_stats": (ctypes.c_int, [_vp, _pi32, _pi32]),
     "pkv_pool_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
+    "pkv_shared_prefix_blocks": (ctypes.c_int, [_vp, _pi32, _i32, _pi32]),
     "pkv_export_state": (ctypes.c_int, [_vp, _pi32, _pi32, _pi32]),
     "pkv_reshape_and_cache": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp]),
     "pkv_copy_blocks": (ctypes.c_int, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, _i32, _vp]),
@@ -76,6 +77,9 @@ _SIGS = {
     "pkv_paged_decode_window": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
                                                _i32, _i32, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
+    "pkv_paged_decode_shared_prefix": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
+                                                      _i32, _vp, _sz, _vp]),
+    "pkv_decode_shared_prefix_workspace_bytes": (_sz, [_vp, _i32, _i32, _i32]),
     "pkv_reshape_and_cache_fp8": (ctypes.c_int, [_vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "pkv_copy_blocks_fp8": (ctypes.c_int, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                            ctypes.POINTER(_vp), _vp, _i32, _vp]),
@@ -294,6 +298,14 @@ class Pool:
         _check(lib.pkv_block_table(self._h, _i32p(s), s.size, _i32p(tables), _i32p(lens)), "pkv_block_table")
         return tables[:s.size], lens[:s.size]
 
+    def shared_prefix_blocks(self, seqs: Sequence[int]) -> int:
+        """pkv_shared_prefix_blocks: leading full blocks that all of `seqs` share physically."""
+        s = np.ascontiguousarray(list(seqs), dtype=np.int32)
+        out = _i32(0)
+        _check(lib.pkv_shared_prefix_blocks(self._h, _i32p(s), s.size, ctypes.byref(out)),
+               "pkv_shared_prefix_blocks")
+        return out.value
+
     def stats(self) -> dict:
         st = Stats()
         _check(lib.pkv_pool_stats(self._h, ctypes.byref(st)), "pkv_pool_stats")
@@ -338,6 +350,21 @@ class Pool:
         _check(lib.pkv_paged_decode(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache), _dev(block_tables),
                                     _dev(context_lens), n_seqs, num_q_heads, float(scale), int(partition_tokens),
                                     _dev(workspace), ws_bytes, _stream(stream)), "pkv_paged_decode")
+
+    def shared_prefix_workspace_bytes(self, n_seqs: int, num_q_heads: int, prefix_blocks: int) -> int:
+        return int(lib.pkv_decode_shared_prefix_workspace_bytes(self._h, int(n_seqs), int(num_q_heads),
+                                                                int(prefix_blocks)))
+
+    def paged_decode_shared_prefix(self, out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                   prefix_blocks: int, workspace=None, stream=None) -> None:
+        """pkv_paged_decode_shared_prefix: decode for a batch whose tables all start with the same
+        prefix_blocks blocks; the shared part is read once for the batch."""
+        n_seqs, num_q_heads = int(q.shape[0]), int(q.shape[1])
+        ws_bytes = 0 if workspace is None else int(workspace.numel() * workspace.element_size())
+        _check(lib.pkv_paged_decode_shared_prefix(self._h, _dev(out), _dev(q), _dev(k_cache), _dev(v_cache),
+                                                  _dev(block_tables), _dev(context_lens), n_seqs, num_q_heads,
+                                                  float(scale), int(prefix_blocks), _dev(workspace), ws_bytes,
+                                                  _stream(stream)), "pkv_paged_decode_shared_prefix")
 
     def reshape_and_cache_fp8(self, k, v, slots, k_cache, v_cache, k_scale, v_scale, stream=None) -> None:
         n = int(slots.shape[0])

@@ -70,7 +70,20 @@ struct DecodeArgs {
   const float* v_scale;
   unsigned long long tag;        // 48-bit tag of this call for ws_count
   unsigned int* err;             // error word of the call's pool (null: the process-wide word)
+  int32_t start;                 // > 0 (a multiple of 16): attend only to positions >= start
+  float* lse_out;                // optional [n_seqs][Hq]: log2 of the softmax denominator of each row, in
+                                 // log2 units of the scaled scores (m + log2 l); -inf for an empty row
+  int32_t* defer_meta;           // balanced mode, non-null: dynamic tasks and no merging here (no fences, no
+                                 // arrivals): each segment of a unit cut by task boundaries leaves its
+                                 // partial in its slot, and block 0 writes [T, pref[0..n]] here for the
+                                 // later kernel that merges them
+  int32_t max_tasks;             // deferred mode: slots for at most this many tasks (2 per task)
+  int32_t early_trigger;         // non-zero: the next kernel may launch once this one passed its own wait
+  int32_t late_wait;             // non-zero: this kernel reads nothing the previous kernel writes (that one let
+                                 // it launch once its own inputs were complete); it waits for the previous
+                                 // kernel only before it completes
 };
+
 
 // Arrival of one segment of a split unit. Returns true for the warp that completes the unit.
 // Lock-free: the CAS only fails when another segment arrived in between.
@@ -95,6 +108,28 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned lo
     old = atomicCAS(ctr, assumed, next);
   } while (old != assumed);
   return static_cast<int64_t>(next & 0xffffull) == n_parts;
+}
+
+// Take k consecutive dynamic tasks of a deferred-mode decode; returns the first index. The counter
+// holds (call tag << 16) | count. A value left by an earlier call (another tag, or fresh memory) is
+// replaced by this call's tag with count k by whichever taker gets there first, which takes index 0.
+// Returns `none` (and records PKV_ERR_DEVICE_TIMEOUT) if the counter could not be taken in a bounded
+// number of tries.
+__device__ __forceinline__ int64_t grab_tasks(unsigned long long* ctr, unsigned long long tag, unsigned int k,
+                                              int64_t none) {
+  unsigned long long cur = ld_relaxed_gpu(ctr);
+  for (int it = 0; it < 256; ++it) {
+    if ((cur >> 16) == tag) {
+      const unsigned long long v = atomicAdd(ctr, static_cast<unsigned long long>(k));
+      if ((v >> 16) == tag) return static_cast<int64_t>(v & 0xffffull);
+      cur = v + k;   // (cannot happen once installed: tags never go back)
+    }
+    const unsigned long long prev = atomicCAS(ctr, cur, (tag << 16) | k);
+    if (prev == cur) return 0;
+    cur = prev;
+  }
+  record_error(ERRBIT_TIMEOUT);
+  return none;
 }
 
 // Log-sum-exp merge of one unit's n_parts segments by one warp. Segment k's slot is
@@ -142,54 +177,57 @@ __device__ __noinline__ void merge_unit(const DecodeArgs& a, int32_t b, int32_t 
       const float inv = 1.f / wsum;
       reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[idx - j * (D / 4)] =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (a.lse_out != nullptr && idx == j * (D / 4)) a.lse_out[static_cast<int64_t>(b) * a.Hq + h * G + j] = M + log2f(wsum);
     }
-    return;
-  }
-  float M[R], wsum[R];
-  float4 acc[R];
+  } else {
+    float M[R], wsum[R];
+    float4 acc[R];
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    M[r] = -INFINITY;
-    wsum[r] = 0.f;
-    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+    for (int r = 0; r < R; ++r) {
+      M[r] = -INFINITY;
+      wsum[r] = 0.f;
+      acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll 2
-  for (int64_t k = 0; k < n_parts; ++k) {
-    const int64_t s = slot_of(k);
-    float2 ml[R];
-    float4 o[R];
+    for (int64_t k = 0; k < n_parts; ++k) {
+      const int64_t s = slot_of(k);
+      float2 ml[R];
+      float4 o[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {  // all of this segment's loads first (L2: written by other warps)
-      const int idx = lane + 32 * r;
-      if (idx < V4) {
-        const int j = idx / (D / 4);
-        ml[r] = ld_part<kCta>(reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2));
-        o[r] = ld_part<kCta>(reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D) + (idx - j * (D / 4)));
+      for (int r = 0; r < R; ++r) {  // all of this segment's loads first (L2: written by other warps)
+        const int idx = lane + 32 * r;
+        if (idx < V4) {
+          const int j = idx / (D / 4);
+          ml[r] = ld_part<kCta>(reinterpret_cast<const float2*>(a.ws_ml + (s * G + j) * 2));
+          o[r] = ld_part<kCta>(reinterpret_cast<const float4*>(a.ws_o + (s * G + j) * D) + (idx - j * (D / 4)));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (lane + 32 * r < V4) {
+          const float Mn = fmaxf(M[r], ml[r].x);
+          const float c = exp2f(M[r] - Mn);  // rescales what was accumulated so far (0 at the start)
+          const float wk = ml[r].y * exp2f(ml[r].x - Mn);
+          acc[r].x = fmaf(wk, o[r].x, acc[r].x * c);
+          acc[r].y = fmaf(wk, o[r].y, acc[r].y * c);
+          acc[r].z = fmaf(wk, o[r].z, acc[r].z * c);
+          acc[r].w = fmaf(wk, o[r].w, acc[r].w * c);
+          wsum[r] = fmaf(wsum[r], c, wk);
+          M[r] = Mn;
+        }
       }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      if (lane + 32 * r < V4) {
-        const float Mn = fmaxf(M[r], ml[r].x);
-        const float c = exp2f(M[r] - Mn);  // rescales what was accumulated so far (0 at the start)
-        const float wk = ml[r].y * exp2f(ml[r].x - Mn);
-        acc[r].x = fmaf(wk, o[r].x, acc[r].x * c);
-        acc[r].y = fmaf(wk, o[r].y, acc[r].y * c);
-        acc[r].z = fmaf(wk, o[r].z, acc[r].z * c);
-        acc[r].w = fmaf(wk, o[r].w, acc[r].w * c);
-        wsum[r] = fmaf(wsum[r], c, wk);
-        M[r] = Mn;
+      const int idx = lane + 32 * r;
+      if (idx < V4) {
+        const int j = idx / (D / 4);
+        const float inv = 1.f / wsum[r];
+        reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[idx - j * (D / 4)] =
+            make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
+        if (a.lse_out != nullptr && idx == j * (D / 4))
+          a.lse_out[static_cast<int64_t>(b) * a.Hq + h * G + j] = M[r] + log2f(wsum[r]);
       }
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int idx = lane + 32 * r;
-    if (idx < V4) {
-      const int j = idx / (D / 4);
-      const float inv = 1.f / wsum[r];
-      reinterpret_cast<float4*>(a.out + (static_cast<int64_t>(b) * a.Hq + h * G + j) * D)[idx - j * (D / 4)] =
-          make_float4(acc[r].x * inv, acc[r].y * inv, acc[r].z * inv, acc[r].w * inv);
     }
   }
 }
@@ -290,12 +328,20 @@ __device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref,
 #pragma unroll
     for (int k = 0; k < kPrefixBatch; ++k) {
       if (base + k * nt >= n) break;  // uniform across the CTA
+      const int32_t b = base + k * nt + tid;
       int32_t len = raw[k];
       if (len < 0 || len > cap) {
         record_error(ERRBIT_BOUNDS);
         len = len < 0 ? 0 : cap;
       }
-      const int32_t c0 = (a.window > 0 && len > a.window) ? (len - a.window) / kChunk : 0;
+      int32_t c0 = (a.window > 0 && len > a.window) ? (len - a.window) / kChunk : 0;
+      if (a.start > 0) {   // positions before `start` belong to another call (a shared prefix)
+        if (len < a.start) {   // (threads past the last sequence hold 0: no chunks, no error)
+          if (b < n) record_error(ERRBIT_BOUNDS);
+          len = a.start;
+        }
+        c0 = max(c0, a.start / kChunk);
+      }
       const int32_t c = (len + kChunk - 1) / kChunk - c0;
       const int32_t ci = (c + PC - 1) / PC;
       int32_t ic = c, ii = ci;  // inclusive warp scan
@@ -323,7 +369,6 @@ __device__ __forceinline__ void build_prefix(const DecodeArgs& a, int32_t* pref,
         tc += sc;
         ti += si;
       }
-      const int32_t b = base + k * nt + tid;
       if (b < n) {
         pref[b] = carry_c + pc + ic - c;
         if (ipref) ipref[b] = carry_i + pi + ii - ci;
@@ -465,7 +510,7 @@ struct SimtMath {
   }
 
   // Writes o / l for the G heads to dst[G][D]; if ml != nullptr also (m, l) to ml[G][2].
-  __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
+  __device__ static void finish(Regs& r, float* dst, float* ml, float* lse, int lane) {
     const int tg = lane / LPT;
     const int cl = lane % LPT;
 #pragma unroll
@@ -495,6 +540,7 @@ struct SimtMath {
         ml[2 * j] = r.m[j];
         ml[2 * j + 1] = lt;
       }
+      if (lse != nullptr && cl == 0) lse[j] = r.m[j] + log2f(lt);
     }
   }
 };
@@ -673,7 +719,7 @@ struct MmaMath {
     }
   }
 
-  __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
+  __device__ static void finish(Regs& r, float* dst, float* ml, float* lse, int lane) {
     const int g = lane >> 2, t = lane & 3;
     float lt0 = r.l[0], lt1 = r.l[1];
 #pragma unroll
@@ -712,6 +758,10 @@ struct MmaMath {
         ml[2 * hd1] = r.m[1];
         ml[2 * hd1 + 1] = lt1;
       }
+    }
+    if (lse != nullptr && g == 0) {
+      if (w0) lse[hd0] = r.m[0] + log2f(lt0);
+      if (w1) lse[hd1] = r.m[1] + log2f(lt1);
     }
   }
 };
@@ -906,7 +956,7 @@ struct Fp8Math {
     }
   }
 
-  __device__ static void finish(Regs& r, float* dst, float* ml, int lane) {
+  __device__ static void finish(Regs& r, float* dst, float* ml, float* lse, int lane) {
     const int g = lane >> 2, t = lane & 3;
     float lt0 = r.l[0], lt1 = r.l[1];
 #pragma unroll
@@ -946,9 +996,186 @@ struct Fp8Math {
         ml[2 * hd1 + 1] = lt1;
       }
     }
+    if (lse != nullptr && g == 0) {
+      if (w0) lse[hd0] = r.m[0] + log2f(lt0);
+      if (w1) lse[hd1] = r.m[1] + log2f(lt1);
+    }
   }
 };
 
+
+// Tasks of a deferred-mode decode: about NP / min_chunks, each more than S chunks (the producer then
+// runs at most one task ahead of the consumer), at most max_tasks.
+__device__ __forceinline__ int64_t defer_task_count(int64_t NP, int32_t min_chunks, int S, int32_t max_tasks) {
+  const int64_t tc = min_chunks > S + 1 ? min_chunks : S + 1;
+  const int64_t T = NP / tc;
+  return T < 1 ? 1 : (T > max_tasks ? max_tasks : T);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Deferred-merge decode of one warp (balanced mode, defer_meta set): dynamic tasks, no merging.
+// The flat chunk list (NP chunks) is cut into T tasks at fixed boundaries NP t / T, so the segments
+// of a task, and their slots 2 t (the task's first segment) and 2 t + 1 (its last), do not depend on
+// which warp runs it. Every task is taken from the call's counter (a CTA's first tasks, one per
+// warp, by one atomic), so CTAs that start late (their SM was still busy) or warps that get slower
+// memory service take fewer, and CTAs that start after the last task was taken do nothing. A unit that one task holds whole is final: its rows go to `out` (and
+// lse_out). Every other segment leaves its partial in its slot for the kernel that follows, which
+// finds them from [T, pref[0..n]] (written here by block 0). The producer runs on into the next
+// task without draining the ring: tasks hold more than S chunks, so it is at most one task ahead.
+// ------------------------------------------------------------------------------------------------
+template <class Math, int D, int G>
+__device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMaps& maps, unsigned char* ring,
+                                                uint64_t* bars, const int32_t* pref, const int32_t* cfirst,
+                                                int64_t NP, int64_t first_task, int lane) {
+  constexpr int SB = Math::kStageBytes;
+  const int S = a.stages;
+  const int32_t n = a.n_seqs, Hkv = a.Hkv;
+  const int64_t T = defer_task_count(NP, a.min_chunks, S, a.max_tasks);
+  if (NP == 0) return;
+  auto t_lo = [&](int64_t t) { return NP * t / T; };
+  auto next_task = [&]() -> int64_t {
+    long long t = 0;
+    if (lane == 0) t = grab_tasks(a.ws_count, a.tag, 1u, T);
+    return __shfl_sync(0xffffffffu, t, 0);
+  };
+  int64_t ctk = first_task;   // the consumer's task
+  if (ctk >= T) return;
+
+  // --- producer: (p_pg, p_sub) = page and chunk within the page of pf; ntk = task after ctk ---
+  const int32_t cpb = a.B / kChunk;
+  Cursor pf = locate(pref, n, Hkv, t_lo(ctk));
+  int64_t p_left = t_lo(ctk + 1) - t_lo(ctk);
+  int64_t ntk = T;
+  bool p_done = false;
+  int32_t p_pg = 0, p_sub = 0;
+  auto p_unit_start = [&]() {
+    const int32_t ch = (cfirst ? cfirst[pf.b] : 0) + pf.c;
+    p_pg = ch / cpb;
+    p_sub = ch - p_pg * cpb;
+    constexpr int kQLines = (G * D * Math::kQElem + 127) / 128;
+    if (lane < kQLines)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const unsigned char*>(a.q) +
+                                                    ((static_cast<int64_t>(pf.b) * a.Hq + pf.h * G) * D) * Math::kQElem +
+                                                    128 * lane));
+  };
+  p_unit_start();
+  int32_t win_b = -1, win_base = 0, win_val = -1;
+  const uint64_t policy = policy_evict_first();
+  int64_t issued = 0;
+  auto issue = [&](int stage) {
+    if (pf.b != win_b || p_pg < win_base || p_pg >= win_base + 32) {
+      win_b = pf.b;
+      win_base = p_pg;
+      const int32_t idx = win_base + lane;
+      win_val = idx < a.MB ? __ldg(a.block_tables + static_cast<int64_t>(pf.b) * a.MB + idx) : -1;
+    }
+    const int32_t blk = __shfl_sync(0xffffffffu, win_val, p_pg - win_base);
+    if (lane == 0) {
+      const uint32_t bar = smem_addr(bars + stage);
+      if (blk >= 0 && blk < a.NB) {
+        const int64_t row0 = (static_cast<int64_t>(blk) * Hkv + pf.h) * a.B + p_sub * kChunk;
+        fence_proxy_async_smem();
+        Math::issue(a, maps, smem_addr(ring + static_cast<size_t>(stage) * SB), bar, row0, policy);
+      } else {
+        record_error(ERRBIT_BOUNDS);
+        mbar_arrive(bar);  // completes the phase with no data; the chunk's result is garbage
+      }
+    }
+    ++issued;
+    if (--p_left > 0) {
+      if (pf.c + 1 < pf.nch) {
+        ++pf.c;
+        if (++p_sub == cpb) {
+          p_sub = 0;
+          ++p_pg;
+        }
+      } else {
+        advance(pf, pref, n, Hkv);
+        p_unit_start();
+      }
+    } else {   // this task is issued: take the next one (the consumer's next task)
+      ntk = next_task();
+      if (ntk < T) {
+        pf = locate(pref, n, Hkv, t_lo(ntk));
+        p_left = t_lo(ntk + 1) - t_lo(ntk);
+        p_unit_start();
+      } else {
+        p_done = true;
+      }
+    }
+  };
+  for (int s = 0; s < S && !p_done; ++s) issue(s);
+
+  // --- consumer ---
+  Cursor cc = locate(pref, n, Hkv, t_lo(ctk));
+  int64_t c_left = t_lo(ctk + 1) - t_lo(ctk);
+  typename Math::Regs r;
+  int32_t seg_c0 = cc.c;
+  int seg_idx = 0;
+  int stage = 0;
+  uint32_t phase = 0;
+  int32_t len_b = clamped_len(a, cc.b);
+  Math::load_q(r, a, cc.b, cc.h, lane);
+  Math::reset(r);
+  int64_t consumed = 0;
+  bool aborted = false;
+  while (true) {
+    if (!mbar_wait_bounded(smem_addr(bars + stage), phase)) {
+      aborted = true;
+      break;
+    }
+    const int32_t tok_abs = ((cfirst ? cfirst[cc.b] : 0) + cc.c) * kChunk;
+    const int32_t vhi = min(kChunk, len_b - tok_abs);
+    const int32_t vlo = a.window > 0 ? max(0, len_b - a.window - tok_abs) : 0;
+    if (!Math::kMaskVariants || vlo > 0 || vhi < kChunk)
+      Math::template chunk<true>(r, ring + static_cast<size_t>(stage) * SB, vlo, vhi, a.scale_log2, lane);
+    else
+      Math::template chunk<false>(r, ring + static_cast<size_t>(stage) * SB, vlo, vhi, a.scale_log2, lane);
+    __syncwarp();
+    ++consumed;
+    if (!p_done) issue(stage);
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    const bool unit_end = (cc.c + 1 == cc.nch);
+    const bool task_end = (c_left == 1);
+    if (unit_end || task_end) {
+      if (seg_c0 == 0 && unit_end) {   // the task holds the whole unit: final rows
+        Math::finish(r, a.out + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G) * D, nullptr,
+                     a.lse_out ? a.lse_out + static_cast<int64_t>(cc.b) * a.Hq + cc.h * G : nullptr, lane);
+      } else {
+        const int64_t slot = 2 * ctk + (seg_idx == 0 ? 0 : 1);
+        Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, nullptr, lane);
+      }
+      ++seg_idx;
+    }
+    if (--c_left > 0) {
+      const int32_t prev_b = cc.b;
+      advance(cc, pref, n, Hkv);
+      if (unit_end) {
+        if (cc.b != prev_b) len_b = clamped_len(a, cc.b);
+        Math::load_q(r, a, cc.b, cc.h, lane);
+        Math::reset(r);
+        seg_c0 = cc.c;
+      }
+    } else {
+      if (ntk >= T) break;   // the producer found no task after this one
+      ctk = ntk;
+      cc = locate(pref, n, Hkv, t_lo(ctk));
+      c_left = t_lo(ctk + 1) - t_lo(ctk);
+      seg_c0 = cc.c;
+      seg_idx = 0;
+      len_b = clamped_len(a, cc.b);
+      Math::load_q(r, a, cc.b, cc.h, lane);
+      Math::reset(r);
+    }
+  }
+  if (aborted) {   // drain the copies still in flight, each with one more bounded wait
+    for (int64_t k = consumed; k < issued; ++k)
+      mbar_wait_bounded(smem_addr(bars + static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1));
+  }
+}
 
 // ------------------------------------------------------------------------------------------------
 // The decode kernel: prefix of chunk counts, even split of the flat chunk list over warps, a
@@ -972,7 +1199,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   int32_t* wsum = reinterpret_cast<int32_t*>(smem + decode_ring_bytes(NW, S, SB) + static_cast<size_t>(NW) * S * 8);
   int32_t* pref = wsum + 64;
   int32_t* ipref = PC > 0 ? pref + (n + 1) : nullptr;
-  int32_t* cfirst = a.window > 0 ? pref + (PC > 0 ? 2 : 1) * (n + 1) : nullptr;
+  int32_t* cfirst = (a.window > 0 || a.start > 0) ? pref + (PC > 0 ? 2 : 1) * (n + 1) : nullptr;
 
   // Arrival counters of split units whose segments all belong to this CTA, indexed by the unit's
   // first warp within the CTA (a warp is the first warp of at most one split unit). wsum[16..24) is
@@ -980,7 +1207,8 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   int32_t* cta_cnt = wsum + 16;
   if (threadIdx.x < NW) cta_cnt[threadIdx.x] = 0;
   set_error_word(a.err);
-  pdl_wait();
+  if (!a.late_wait) pdl_wait();
+  if (a.early_trigger) pdl_launch_dependents();
   build_prefix(a, pref, ipref, cfirst, wsum);
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
@@ -992,11 +1220,13 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   const int w = blockIdx.x * NW + warp;
   const int64_t NP = static_cast<int64_t>(pref[n]) * Hkv;
 
-  // Empty sequences: zero rows.
+  // Empty sequences: zero rows (and a log-sum-exp of -inf: no weight in a later merge).
   for (int32_t b = w; b < n; b += W) {
     if (pref[b + 1] != pref[b]) continue;
     float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(b) * a.Hq * D);
     for (int i = lane; i < a.Hq * D / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.lse_out != nullptr)
+      for (int i = lane; i < a.Hq; i += 32) a.lse_out[static_cast<int64_t>(b) * a.Hq + i] = -INFINITY;
   }
 
   // Balanced mode splits the chunks over Weff = min(W, max(1, NP / mc)) warps, mc = min_chunks (half
@@ -1006,6 +1236,23 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   const int64_t mc = NP < 8192 ? (a.min_chunks + 1) / 2 : a.min_chunks;  // small problems: shorter ranges
   const int64_t Wmax = NP / mc > 0 ? NP / mc : 1;
   const int64_t Weff = Wmax < W ? Wmax : W;
+  if (a.defer_meta != nullptr) {
+    const int64_t T = defer_task_count(NP, a.min_chunks, S, a.max_tasks);
+    if (blockIdx.x == 0) {   // where the merging kernel finds each unit's parts
+      for (int32_t i = threadIdx.x; i <= n; i += blockDim.x) a.defer_meta[1 + i] = pref[i];
+      if (threadIdx.x == 0) a.defer_meta[0] = static_cast<int32_t>(T);
+    }
+    // the CTA's first tasks, one per warp, in one atomic (wsum[8] is free after the prefix build)
+    if (threadIdx.x == 0) {
+      const int64_t t0 = NP > 0 ? grab_tasks(a.ws_count, a.tag, static_cast<unsigned int>(NW), T) : T;
+      wsum[8] = static_cast<int32_t>(t0 < T ? t0 : T);
+    }
+    __syncthreads();
+    decode_deferred<Math, D, G>(a, maps, ring, bars, pref, cfirst, NP, static_cast<int64_t>(wsum[8]) + warp, lane);
+    if (a.late_wait) pdl_wait();
+    pdl_launch_dependents();
+    return;
+  }
   int64_t lo, hi;
   if (PC == 0) {
     if (w >= Weff) return;
@@ -1149,7 +1396,8 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     if (unit_end || part_end || range_end) {
       const bool complete = (seg_c0 == 0) && unit_end;
       if (complete) {
-        Math::finish(r, a.out + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G) * D, nullptr, lane);
+        Math::finish(r, a.out + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G) * D, nullptr,
+                     a.lse_out ? a.lse_out + static_cast<int64_t>(cc.b) * a.Hq + cc.h * G : nullptr, lane);
       } else {
         const int64_t u = static_cast<int64_t>(cc.b) * Hkv + cc.h;
         const int64_t slot = (PC == 0) ? (2 * static_cast<int64_t>(w) + (seg_idx == 0 ? 0 : 1))
@@ -1169,9 +1417,11 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
         }
         const bool intra = (PC == 0) && (wf / NW == (wf + n_parts - 1) / NW);
         if (pub) publish();
-        if (intra) {
+        if (a.defer_meta != nullptr) {   // merged by a later kernel
+          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, nullptr, lane);
+        } else if (intra) {
           // all segments in this CTA: CTA-scope release / acquire around a shared-memory count
-          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
+          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, nullptr, lane);
           __syncwarp();
           fence_acq_rel_cta();
           int last = 0;
@@ -1199,7 +1449,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
           }
           others = __shfl_sync(0xffffffffu, others, 0);
           if (others) fence_acq_rel_gpu();  // the other segments' partials are read after this point
-          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
+          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, nullptr, lane);
           int mine = others;
           if (!others) {
             __syncwarp();
@@ -1218,7 +1468,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
             pend_kind = first_kind;
           }
         } else {
-          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, lane);
+          Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, nullptr, lane);
           pub = true;
           pub_wait = kPubDelay;
           pub_b = cc.b;
@@ -1259,6 +1509,129 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
       if (lane == 0) a.ws_count[static_cast<int64_t>(pend_b) * Hkv + pend_h] = 0ull;   // every part has arrived
     }
   }
+}
+
+// Shared-prefix (cascade) merge. A batch whose sequences all begin with the same prefix_blocks
+// physical blocks is attended in two parts: each sequence's private suffix by the decode kernel in
+// deferred-merge mode (rows of units that one warp finished are final in `out` with their log-sum-exp
+// lse_s; units split over warps left one partial per warp in the decode workspace), and the shared
+// prefix once for all rows by the tensor-core prefill kernel in shared-prefix mode (n_split key
+// splits, part_o / part_lse). The exact attention over the whole context is the log-sum-exp
+// combination of all those parts ("Servicio de modelos de lenguaje con un presupuesto de memoria" §6:
+// blockwise exact attention with running statistics):
+//     M = max_k lse_k, w_k = 2^(lse_k - M), out = sum_k w_k o_k / sum_k w_k   (each o_k normalised).
+// One warp per (sequence, query head) row, the loads of 4 parts in flight at a time. The kernel also
+// checks that every table of the call begins with sequence 0's first prefix_blocks entries (else
+// PKV_ERR_DEVICE_BOUNDS).
+struct CascadeMergeArgs {
+  float* out;
+  const float* lse_s;       // [n_rows] suffix log-sum-exp of rows whose unit was not split
+  const float* part_o;      // [n_split][n_rows][D] prefix partials (normalised)
+  const float* part_lse;    // [n_split][n_rows]
+  const float* dec_o;       // decode slots [2 W][G][D] (normalised)
+  const float* dec_ml;      // decode slots [2 W][G][2] (m, l)
+  const int32_t* meta;      // [T, pref[0..n]] written by the decode
+  unsigned long long* task_ctr;   // the decode's task counter: zeroed here (CUDA-graph replays reuse the call tag)
+  const int32_t* tables;
+  int64_t n_rows;
+  int32_t D, G, Hkv, n_split, MB, n_seqs, prefix_blocks;
+  unsigned int* err;
+};
+
+__global__ void __launch_bounds__(256, 4) merge_prefix_kernel(const __grid_constant__ CascadeMergeArgs a) {
+  set_error_word(a.err);
+  pdl_wait();
+  const int64_t gthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gtid == 0) *a.task_ctr = 0ull;   // the decode has completed: every task was taken
+  for (int64_t i = gtid; i < static_cast<int64_t>(a.n_seqs) * a.prefix_blocks; i += gthreads) {
+    const int64_t b = i / a.prefix_blocks, k = i - b * a.prefix_blocks;
+    if (__ldg(a.tables + b * a.MB + k) != __ldg(a.tables + k)) record_error(ERRBIT_BOUNDS);
+  }
+  const int lane = threadIdx.x & 31;
+  const int D = a.D, Hq = a.Hkv * a.G;
+  const bool has_c = lane < D / 4;                 // this lane's float4 of the row
+  const int64_t T = __ldg(a.meta);   // the decode's task count
+  const int32_t* pref = a.meta + 1;
+  const int64_t NP = static_cast<int64_t>(__ldg(pref + a.n_seqs)) * a.Hkv;
+  constexpr int kBatch = 4;
+  for (int64_t row = gtid >> 5; row < a.n_rows; row += gthreads >> 5) {
+    const int32_t b = static_cast<int32_t>(row / Hq), j = static_cast<int32_t>(row - static_cast<int64_t>(b) * Hq);
+    const int32_t h = j / a.G, jj = j - h * a.G;
+    // the suffix parts of the row: none (empty suffix), the final row (unit of one task), or one
+    // partial per task of a cut unit (task boundaries NP t / T: task_of(p) = floor(((p + 1) T - 1) / NP))
+    const int64_t nch = __ldg(pref + b + 1) - __ldg(pref + b);
+    int64_t wf = 0, n_suf = 0;
+    int first_kind = 0;
+    if (nch > 0) {
+      const int64_t s_u = static_cast<int64_t>(__ldg(pref + b)) * a.Hkv + h * nch, e_u = s_u + nch;
+      wf = ((s_u + 1) * T - 1) / NP;
+      n_suf = (e_u * T - 1) / NP - wf + 1;
+      first_kind = (s_u == NP * wf / T) ? 0 : 1;
+    }
+    const bool whole = n_suf == 1;
+    const int64_t n_parts = (n_suf > 1 ? n_suf : 0) + a.n_split;
+    // part p < n_suf: decode slot of the split unit's p-th segment; then the prefix splits
+    auto part_lse = [&](int64_t p) -> float {
+      if (p < n_parts - a.n_split) {
+        const int64_t slot = 2 * (wf + p) + (p == 0 ? first_kind : 0);
+        const float2 ml = __ldg(reinterpret_cast<const float2*>(a.dec_ml) + slot * a.G + jj);
+        return ml.x + log2f(ml.y);
+      }
+      return __ldg(a.part_lse + (p - (n_parts - a.n_split)) * a.n_rows + row);
+    };
+    auto part_o = [&](int64_t p) -> const float4* {
+      if (p < n_parts - a.n_split) {
+        const int64_t slot = 2 * (wf + p) + (p == 0 ? first_kind : 0);
+        return reinterpret_cast<const float4*>(a.dec_o + (slot * a.G + jj) * D);
+      }
+      return reinterpret_cast<const float4*>(a.part_o + ((p - (n_parts - a.n_split)) * a.n_rows + row) * D);
+    };
+    const float ls = whole ? __ldg(a.lse_s + row) : -INFINITY;
+    float M = ls;
+    for (int64_t k0 = 0; k0 < n_parts; k0 += 32) {
+      float v = k0 + lane < n_parts ? part_lse(k0 + lane) : -INFINITY;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+      M = fmaxf(M, v);
+    }
+    const float ws = whole ? exp2f(ls - M) : 0.f;
+    float wsum = ws;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (whole && has_c) {
+      const float4 so = reinterpret_cast<const float4*>(a.out + row * D)[lane];
+      acc = make_float4(ws * so.x, ws * so.y, ws * so.z, ws * so.w);
+    }
+    for (int64_t k0 = 0; k0 < n_parts; k0 += 32) {
+      const int nk = static_cast<int>(n_parts - k0 < 32 ? n_parts - k0 : 32);
+      const float wl = lane < nk ? exp2f(part_lse(k0 + lane) - M) : 0.f;
+      float t = wl;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      wsum += t;
+      for (int jb = 0; jb < nk; jb += kBatch) {
+        float4 v[kBatch];
+        float wj[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          wj[u] = __shfl_sync(0xffffffffu, wl, (jb + u) & 31);
+          v[u] = (has_c && jb + u < nk) ? __ldg(part_o(k0 + jb + u) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          acc.x = fmaf(wj[u], v[u].x, acc.x);
+          acc.y = fmaf(wj[u], v[u].y, acc.y);
+          acc.z = fmaf(wj[u], v[u].z, acc.z);
+          acc.w = fmaf(wj[u], v[u].w, acc.w);
+        }
+      }
+    }
+    if (has_c) {
+      const float inv = 1.f / wsum;
+      reinterpret_cast<float4*>(a.out + row * D)[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+  }
+  pdl_launch_dependents();
 }
 
 }  // namespace pkv_dev

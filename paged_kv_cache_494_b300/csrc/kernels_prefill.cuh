@@ -30,6 +30,17 @@ struct PrefillArgs {
   int32_t n_seqs, Hq, Hkv, B, NB, MB, window, stages;
   float scale_log2;
   unsigned int* err;             // error word of the call's pool (null: the process-wide word)
+  // Shared-prefix mode (tcgen05 kernel only; shared_len > 0): the keys are positions [0, shared_len)
+  // of sequence 0's table, every one of the total_q rows of q attends to all of them (no causal
+  // mask), and the keys are cut into splits of split_keys (a multiple of 64); split s writes its
+  // normalised partial output to part_o[s][row][head][:] and m + log2 l to part_lse[s][row][head].
+  // cu_q and context_lens are not read.
+  int32_t total_q, shared_len, split_keys;
+  float* part_o;
+  float* part_lse;
+  int32_t early_trigger;   // tcgen05 kernel: the next kernel may launch once this one passed its own wait
+  unsigned long long* task_ctr;   // optional: the following decode's task counter, set to its call tag
+  unsigned long long task_tag;    //   here so that its first takers find it installed
 };
 
 template <int D, int G>

@@ -70,14 +70,17 @@ struct TcShape {
   static constexpr int NTB = 7;                     // barriers per tile
   static constexpr int N_BARS = 2 + 2 * STAGES + NTB * NT + 1;
   static constexpr int SOFTMAX_THREADS = 128 * NT;
-  static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;   // tmem base, abort flag, scan scratch, prefix
+  // epilogue staging, per softmax warp: 32 rows x 16 floats (2 KB), 16-byte slots XOR-swizzled
+  static constexpr int EPI_WARP_BYTES = 32 * 16 * 4;
+  static constexpr int EPI_OFF = BAR_OFF + (N_BARS * 8 + 127) / 128 * 128;
+  static constexpr int MISC_OFF = EPI_OFF + 4 * NT * EPI_WARP_BYTES;   // tmem base, abort flag, scan scratch, prefix
   static_assert(D == 64 || D == 128, "D");
   static_assert(G >= 1 && G <= 8, "G");
   static_assert(NT == 1 || NT == 2, "NT");
   static_assert(NT * TCOLS <= 512, "tensor memory");
 };
 
-// [1 KB alignment slack][Q tiles][ring][barriers][tmem base, abort][64-int scan scratch][prefix]
+// [1 KB alignment slack][Q tiles][ring][barriers][epilogue staging][tmem base, abort][64-int scan scratch][prefix]
 template <class Sh>
 __host__ __device__ inline size_t prefill_tc_smem_bytes(int n_seqs) {
   return 1024 + Sh::MISC_OFF + 16 + 256 + static_cast<size_t>(n_seqs + 1) * 4;
@@ -208,6 +211,8 @@ struct TcMaps {
 // One work item of the persistent loop: NT consecutive Q tiles of one (sequence, KV head).
 struct TcItem {
   int32_t b, h, q0, len, pos0, t_begin, t_end, n_act, c_lo, c_hi, kt_lo, n_steps;
+  int32_t fixed_pos;   // shared-prefix mode: the position of every row (shared_len - 1); else -1
+  int32_t split;       // shared-prefix mode: key split of the item
 };
 
 template <int D, int G, int NT, int STAGES>
@@ -239,10 +244,24 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
 
   set_error_word(a.err);
   pdl_wait();   // before any global access, and before holding tensor memory
+  if (a.task_ctr != nullptr && blockIdx.x == 0 && tid == 0) {
+    install_task_tag(a.task_ctr, a.task_tag);
+    __threadfence();
+  }
+  if (a.early_trigger) pdl_launch_dependents();
 
-  // ---- items per sequence (prefix over sequences) and the largest count
+  // ---- items per sequence (prefix over sequences) and the largest count; shared-prefix mode: one
+  // virtual sequence whose queries are all total_q rows
+  const bool shared = a.shared_len > 0;
   if (tid == 0) *max_items = 0;
-  {
+  if (shared) {
+    if (tid == 0) {
+      tpref[0] = 0;
+      tpref[1] = (a.total_q + ITEM - 1) / ITEM;
+      *max_items = tpref[1];
+    }
+    __syncthreads();
+  } else {
     constexpr int nw = NTHR / 32;
     int32_t carry = 0;
     for (int32_t base = 0; base < n; base += NTHR) {
@@ -280,13 +299,36 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
   // Work slots, heaviest first: slot x = (level L, sequence b, KV head h), level-major; level L of
   // sequence b is its item counted from the end (the longest causal range first). CTA c takes slots
   // c, c + gridDim.x, ...; slots past a sequence's item count are empty.
-  const int64_t per_level = static_cast<int64_t>(n) * a.Hkv;
-  const int64_t n_slots = static_cast<int64_t>(*max_items) * per_level;
+  const int64_t per_level = shared ? static_cast<int64_t>(*max_items) * a.Hkv : static_cast<int64_t>(n) * a.Hkv;
+  const int32_t n_split = shared ? (a.shared_len + a.split_keys - 1) / a.split_keys : 1;
+  const int64_t n_slots = shared ? static_cast<int64_t>(n_split) * per_level : static_cast<int64_t>(*max_items) * per_level;
   if (static_cast<int64_t>(blockIdx.x) >= n_slots) {
     pdl_launch_dependents();
     return;
   }
   auto get_item = [&](int64_t x, TcItem& it) -> bool {
+    if (shared) {   // slot = (split, item, KV head): every item of a split has the same key range
+      it.split = static_cast<int32_t>(x / per_level);
+      const int64_t r2 = x - static_cast<int64_t>(it.split) * per_level;
+      const int32_t item = static_cast<int32_t>(r2 / a.Hkv);
+      it.h = static_cast<int32_t>(r2 - static_cast<int64_t>(item) * a.Hkv);
+      it.b = 0;
+      it.q0 = 0;
+      it.len = a.shared_len;
+      it.pos0 = 0;
+      it.fixed_pos = a.shared_len - 1;
+      it.t_begin = item * ITEM;
+      it.t_end = min(it.t_begin + ITEM, a.total_q);
+      it.n_act = (it.t_end - it.t_begin + TQ - 1) / TQ;
+      const int32_t k0 = it.split * a.split_keys, k1 = min(k0 + a.split_keys, a.shared_len);
+      it.c_lo = k0 / kChunk;
+      it.c_hi = (k1 - 1) / kChunk;
+      it.kt_lo = it.c_lo / kTcChunks;
+      it.n_steps = it.c_hi / kTcChunks - it.kt_lo + 1;
+      return true;
+    }
+    it.fixed_pos = -1;
+    it.split = 0;
     const int32_t L = static_cast<int32_t>(x / per_level);
     const int64_t r = x - static_cast<int64_t>(L) * per_level;
     it.b = static_cast<int32_t>(r / a.Hkv);
@@ -323,11 +365,13 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
   auto tile_last_tok = [&](const TcItem& it, int t) { return min(it.t_begin + (t + 1) * TQ, it.t_end) - 1; };
   // step range of tile t within the item's ring steps: [off, off + cnt)
   auto tile_off = [&](const TcItem& it, int t) -> int32_t {
+    if (it.fixed_pos >= 0) return 0;
     const int32_t p = it.pos0 + tile_first_tok(it, t);
     const int32_t c = (a.window > 0 && p - a.window + 1 > 0) ? (p - a.window + 1) / kChunk : 0;
     return c / kTcChunks - it.kt_lo;
   };
   auto tile_cnt = [&](const TcItem& it, int t) -> int32_t {
+    if (it.fixed_pos >= 0) return it.n_steps;
     return (it.pos0 + tile_last_tok(it, t)) / kChunk / kTcChunks - it.kt_lo - tile_off(it, t) + 1;
   };
 
@@ -549,9 +593,9 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
         const int32_t first = tile_first_tok(it, t), last = tile_last_tok(it, t);
         const int32_t tok = min(first + r / G, last);               // padding rows repeat a real token
         const bool row_real = r < ROWS && first + r / G <= last;
-        const int32_t p_r = it.pos0 + tok;
+        const int32_t p_r = it.fixed_pos >= 0 ? it.fixed_pos : it.pos0 + tok;
         const int32_t ws_r = a.window > 0 ? p_r - a.window + 1 : 0;
-        const int32_t p_min = it.pos0 + first;                       // smallest position of the tile
+        const int32_t p_min = it.fixed_pos >= 0 ? it.fixed_pos : it.pos0 + first;   // smallest position of the tile
         const int32_t ws_max = a.window > 0 ? it.pos0 + last - a.window + 1 : 0;
         const int32_t t_off = tile_off(it, t), t_cnt = tile_cnt(it, t);
         float m = -INFINITY, l = 0.f;
@@ -675,16 +719,41 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
         }
         tc_fence_after();
         const float inv = 1.f / l;
-        float* dst = a.out + ((static_cast<int64_t>(it.q0) + tok) * a.Hq + it.h * G + (r % G)) * D;
+        const int64_t orow = (static_cast<int64_t>(it.q0) + tok) * a.Hq + it.h * G + (r % G);
+        float* dst = shared ? a.part_o + (static_cast<int64_t>(it.split) * a.total_q * a.Hq + orow) * D
+                            : a.out + orow * D;
+        if (shared && row_real) a.part_lse[static_cast<int64_t>(it.split) * a.total_q * a.Hq + orow] = m + log2f(l);
+        // Coalesced stores: each 32 x 16 block of the warp's rows goes through shared memory, so that
+        // a store instruction writes 64 contiguous bytes of each of 8 rows (4 lanes per row) instead
+        // of 16 bytes of each of 32 rows. Slot s of row j sits at slot s ^ ((j >> 1) & 3) of that row:
+        // both the row-wise writes and the column-wise reads hit 8 distinct 16-byte bank groups per
+        // quarter warp. rd[i]: destination of row 8 i + lane / 4 (null for a padding row).
+        float4* stg = reinterpret_cast<float4*>(smem + Sh::EPI_OFF + warp * Sh::EPI_WARP_BYTES);
+        float* rd[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          rd[i] = reinterpret_cast<float*>(__shfl_sync(
+              0xffffffffu, reinterpret_cast<unsigned long long>(row_real ? dst : nullptr), 8 * i + (lane >> 2)));
+        const int sl = lane & 3;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float o[32];
           tmem_ld32(tm + c, o);
-          if (row_real) {
 #pragma unroll
-            for (int k2 = 0; k2 < 32; k2 += 4)
-              *reinterpret_cast<float4*>(dst + c + k2) =
-                  make_float4(o[k2] * inv, o[k2 + 1] * inv, o[k2 + 2] * inv, o[k2 + 3] * inv);
+          for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              const float* v = o + 16 * hf + 4 * s4;
+              stg[lane * 4 + (s4 ^ ((lane >> 1) & 3))] = make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int row = 8 * i + (lane >> 2);
+              const float4 v = stg[row * 4 + (sl ^ ((row >> 1) & 3))];
+              if (rd[i] != nullptr) *reinterpret_cast<float4*>(rd[i] + c + 16 * hf + 4 * sl) = v;
+            }
+            __syncwarp();
           }
         }
       }

@@ -12,6 +12,7 @@
 // The orderings the pages leave open (free-list order, id choice, when a copy fires) are fixed in
 // include/pagedkv.h.
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <unordered_map>
@@ -383,6 +384,25 @@ pkv_status pkv_block_table(const pkv_pool* p, const int32_t* seqs, int32_t n, in
     }
     if (lens_out) lens_out[i] = p->lens[seqs[i]];
   }
+  return PKV_OK;
+}
+
+pkv_status pkv_shared_prefix_blocks(const pkv_pool* p, const int32_t* seqs, int32_t n, int32_t* out_blocks) {
+  if (!p || n <= 0 || !seqs || !out_blocks) return PKV_ERR_INVALID;
+  for (int32_t i = 0; i < n; ++i)
+    if (seqs[i] < 0 || seqs[i] >= p->desc.max_seqs || !p->live[seqs[i]]) return PKV_ERR_NO_SEQ;
+  // full blocks of the shortest sequence bound the count; then the first logical block whose
+  // physical id differs between any two sequences ends it
+  int64_t k_max = INT64_MAX;
+  for (int32_t i = 0; i < n; ++i) k_max = std::min<int64_t>(k_max, p->lens[seqs[i]] / p->desc.block_size);
+  const std::vector<int32_t>& t0 = p->tables[seqs[0]];
+  int64_t k = 0;
+  for (; k < k_max; ++k) {
+    bool same = true;
+    for (int32_t i = 1; i < n && same; ++i) same = p->tables[seqs[i]][k] == t0[k];
+    if (!same) break;
+  }
+  *out_blocks = static_cast<int32_t>(k);
   return PKV_OK;
 }
 

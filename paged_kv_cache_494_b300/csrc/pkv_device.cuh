@@ -30,6 +30,19 @@ __device__ __forceinline__ void record_error(unsigned int bit) {
   atomicOr(w ? w : &g_error_bits, bit);
 }
 
+// Makes a tagged task counter ((tag << 16) | count) belong to this call: a value with another tag (an
+// earlier call's, or fresh memory) is replaced by (tag << 16) | 0; a value with this tag is left as it
+// is (takers may already have counted on it). Bounded: gives up quietly, and takers then install the
+// tag themselves.
+__device__ __forceinline__ void install_task_tag(unsigned long long* ctr, unsigned long long tag) {
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+  for (int it = 0; it < 64 && (cur >> 16) != tag; ++it) {
+    const unsigned long long prev = atomicCAS(ctr, cur, tag << 16);
+    if (prev == cur) return;
+    cur = prev;
+  }
+}
+
 // Upper bound on mbarrier polls before a wait gives up. Each try_wait may itself suspend the thread
 // for a hardware-chosen interval (measured on B300: ~4 us per unsatisfied poll), so a stuck wait
 // gives up after about a second of running; a copy in flight completes in microseconds.

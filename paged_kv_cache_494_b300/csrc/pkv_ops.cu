@@ -61,7 +61,9 @@ int num_sms() {
 
 // Programmatic dependent launch on every libpagedkv kernel unless PKV_PDL=0. Each kernel waits for
 // its predecessor in the stream (griddepcontrol.wait) before touching global memory, so only the
-// launch latency overlaps; data ordering is plain stream order.
+// launch latency overlaps and data ordering is plain stream order; the one exception is the
+// shared-prefix decode, whose middle kernel reads nothing its predecessor writes and waits for it
+// only before completing (the tensor-core kernel lets it launch once its own inputs are complete).
 bool pdl_enabled() {
   static const bool on = [] {
     const char* s = std::getenv("PKV_PDL");
@@ -321,9 +323,49 @@ int occupancy(const void* fn, int threads, size_t smem) {
   return per_sm;
 }
 
+// Launches the tcgen05 prefill kernel for the arguments in `a` (items: NT Q tiles of 128 / G tokens;
+// shared-prefix mode when a.shared_len > 0). grid_items: number of work items when known, else -1.
+pkv_status tc_prefill_launch(const pkv_pool* p, const pkv_dev::PrefillArgs& a, const void* k_cache,
+                             const void* v_cache, cudaStream_t st, int64_t grid_items) {
+  const pkv_pool_desc& d = p->desc;
+  const int g = a.Hq / d.num_kv_heads;
+  TcKernel tk;
+#define PKV_TC_CASE(DD, GG) \
+  if (d.head_dim == DD && g == GG) tk = tc_pick<DD, GG, kTcTiles, kTcStages>(a.n_seqs);
+  PKV_TC_CASE(64, 1) PKV_TC_CASE(64, 2) PKV_TC_CASE(64, 3) PKV_TC_CASE(64, 4)
+  PKV_TC_CASE(64, 5) PKV_TC_CASE(64, 6) PKV_TC_CASE(64, 7) PKV_TC_CASE(64, 8)
+  PKV_TC_CASE(128, 1) PKV_TC_CASE(128, 2) PKV_TC_CASE(128, 3) PKV_TC_CASE(128, 4)
+  PKV_TC_CASE(128, 5) PKV_TC_CASE(128, 6) PKV_TC_CASE(128, 7) PKV_TC_CASE(128, 8)
+#undef PKV_TC_CASE
+  if (!tk.kern) return PKV_ERR_INVALID;
+  if (!ensure_smem(reinterpret_cast<const void*>(tk.kern), tk.smem)) return PKV_ERR_CUDA;
+  pkv_dev::TcMaps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d) ||
+      !encode_q_map(&maps.q, a.q, a.total_q, a.Hq, d.head_dim, g))
+    return PKV_ERR_CUDA;
+  // persistent: one CTA per SM (or fewer when there are fewer work items)
+  const int64_t items_ub = grid_items >= 0 ? grid_items
+                                           : ((static_cast<int64_t>(a.total_q) + tk.item - 1) / tk.item + a.n_seqs) *
+                                                 d.num_kv_heads;
+  const int sms = num_sms();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(items_ub < sms ? (items_ub > 0 ? items_ub : 1) : sms);
+  if (launch(tk.kern, dim3(grid), dim3(tk.threads), tk.smem, st, a, maps) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+// Query tokens per tcgen05 prefill work item for a head dimension and group size (0 if unsupported).
+int tc_item_tokens(int D, int g) {
+  if ((D != 64 && D != 128) || g < 1 || g > 8) return 0;
+  return kTcTiles * (pkv_dev::kTcRows / g);
+}
+
 struct DecodePlan {
   KernelPair k;
-  int nw = 4, stages = 2, grid = 0, warps = 0;
+  int nw = 4, stages = 2, grid = 0, warps = 0, max_tasks = 0;
   size_t smem = 0;
   int part_chunks = 0, max_parts = 0;
   int64_t n_units = 0, n_slots = 0;
@@ -356,8 +398,9 @@ size_t max_smem_optin() {
   return static_cast<size_t>(v);
 }
 
+// defer: the deferred-merge mode (dynamic tasks, 2 slots per task, up to 4 tasks per warp).
 pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t partition_tokens, int32_t window,
-                       DecodePlan* out) {
+                       DecodePlan* out, bool defer = false) {
   const pkv_pool_desc& d = p->desc;
   if (n_seqs < 0 || Hq <= 0 || Hq % d.num_kv_heads != 0) return PKV_ERR_INVALID;
   if (d.block_size % pkv_dev::kChunk != 0) return PKV_ERR_INVALID;
@@ -387,6 +430,11 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
     const int64_t max_chunks = (static_cast<int64_t>(d.max_blocks_per_seq) * d.block_size) / pkv_dev::kChunk;
     pl.max_parts = static_cast<int>((max_chunks + pl.part_chunks - 1) / pl.part_chunks);
     pl.n_slots = pl.n_units * pl.max_parts;
+  } else if (defer) {
+    // 16-bit task counts: tasks plus one CTA grab and one final grab per warp stay below 2^16
+    pl.max_tasks = 4 * pl.warps < 60000 - 2 * pl.warps ? 4 * pl.warps : 60000 - 2 * pl.warps;
+    if (pl.max_tasks < 1) return PKV_ERR_INVALID;
+    pl.n_slots = 2 * static_cast<int64_t>(pl.max_tasks);
   } else {
     pl.n_slots = 2 * static_cast<int64_t>(pl.warps);
   }
@@ -403,7 +451,8 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
                          const float* k_scale, const float* v_scale, const int32_t* block_tables,
                          const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads, float scale,
                          int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
-                         void* stream);
+                         void* stream, int32_t start = 0, float* lse_out = nullptr,
+                         int32_t* defer_meta = nullptr, int32_t late_wait = 0, unsigned long long tag = 0);
 
 }  // namespace
 
@@ -480,6 +529,7 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size;
   if (rows > 0x7fffffffLL || d.num_kv_heads > 65535) return PKV_ERR_INVALID;
   pkv_dev::PrefillArgs a;
+  std::memset(&a, 0, sizeof a);   // fields of the shared-prefix mode stay off
   a.out = out;
   a.q = q;
   a.block_tables = block_tables;
@@ -495,37 +545,13 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = p->d_err_word;
   a.stages = 0;   // the tcgen05 kernel fixes its ring depth at compile time
+  a.total_q = total_q;
+  a.shared_len = 0;
+  a.split_keys = 0;
+  a.part_o = nullptr;
+  a.part_lse = nullptr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (prefill_path_tc() && n_seqs <= kPrefillTcMaxSeqs) {
-    // tensor-core path: tcgen05.mma with S, P and O in tensor memory, two 128-row Q tiles per work item
-    TcKernel tk;
-#define PKV_TC_CASE(DD, GG)        \
-    if (d.head_dim == DD && g == GG) tk = tc_pick<DD, GG, kTcTiles, kTcStages>(n_seqs);
-    PKV_TC_CASE(64, 1) PKV_TC_CASE(64, 2) PKV_TC_CASE(64, 3) PKV_TC_CASE(64, 4)
-    PKV_TC_CASE(64, 5) PKV_TC_CASE(64, 6) PKV_TC_CASE(64, 7) PKV_TC_CASE(64, 8)
-    PKV_TC_CASE(128, 1) PKV_TC_CASE(128, 2) PKV_TC_CASE(128, 3) PKV_TC_CASE(128, 4)
-    PKV_TC_CASE(128, 5) PKV_TC_CASE(128, 6) PKV_TC_CASE(128, 7) PKV_TC_CASE(128, 8)
-#undef PKV_TC_CASE
-    auto kern = tk.kern;
-    const size_t smem = tk.smem;
-    const int tq = tk.item;
-    if (!kern) return PKV_ERR_INVALID;
-    if (!ensure_smem(reinterpret_cast<const void*>(kern), smem)) return PKV_ERR_CUDA;
-    pkv_dev::TcMaps maps;
-    std::memset(&maps, 0, sizeof maps);
-    if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d) ||
-        !encode_q_map(&maps.q, q, total_q, num_q_heads, d.head_dim, g))
-      return PKV_ERR_CUDA;
-    // persistent: one CTA per SM (or fewer when there are fewer work items)
-    const int64_t items_ub = ((static_cast<int64_t>(total_q) + tq - 1) / tq + n_seqs) * d.num_kv_heads;
-    const int sms = num_sms();
-    if (sms <= 0) return PKV_ERR_CUDA;
-    const unsigned grid = static_cast<unsigned>(items_ub < sms ? items_ub : sms);
-    if (launch(kern, dim3(grid), dim3(tk.threads), smem, st, a, maps) != cudaSuccess ||
-        cudaGetLastError() != cudaSuccess)
-      return PKV_ERR_CUDA;
-    return PKV_OK;
-  }
+  if (prefill_path_tc() && n_seqs <= kPrefillTcMaxSeqs) return tc_prefill_launch(p, a, k_cache, v_cache, st, -1);
   using PK = void (*)(pkv_dev::PrefillArgs, pkv_dev::TmaMaps);
   PK kern = nullptr;
   int tq = 0, stage_bytes = 0, q_bytes = 0;
@@ -661,7 +687,8 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
                          const float* k_scale, const float* v_scale, const int32_t* block_tables,
                          const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads, float scale,
                          int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+                         void* stream, int32_t start, float* lse_out, int32_t* defer_meta,
+                         int32_t late_wait, unsigned long long tag) {
   if (!p || window < 0) return PKV_ERR_INVALID;
   if (n_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID;
@@ -670,7 +697,9 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
     return PKV_ERR_INVALID;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID;
   DecodePlan pl;
-  const pkv_status st = plan_decode(p, n_seqs, num_q_heads, partition_tokens, window, &pl);
+  const bool defer = defer_meta != nullptr && partition_tokens == 0;
+  const pkv_status st =
+      plan_decode(p, n_seqs, num_q_heads, partition_tokens, (window > 0 || start > 0) ? 1 : 0, &pl, defer);
   if (st != PKV_OK) return st;
   if (workspace_bytes < pl.ws_bytes || (pl.ws_bytes > 0 && (!workspace || !aligned16(workspace))))
     return PKV_ERR_INVALID;
@@ -717,8 +746,16 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   // warps gain (measured on batches of 4-256 sequences of 256-4096 tokens; problems with more than
   // 16 chunks per warp are unaffected).
   a.min_chunks = env_int("PKV_DECODE_MIN_CHUNKS", 16);
-  a.tag = next_call_tag();
+  a.tag = tag != 0 ? tag : next_call_tag();
   a.err = p->d_err_word;
+  a.start = start;
+  a.lse_out = lse_out;
+  a.defer_meta = defer ? defer_meta : nullptr;
+  a.max_tasks = pl.max_tasks;
+  // deferred mode: chunks per task (no arrivals, so cutting units costs no fences; small tasks balance)
+  if (defer) a.min_chunks = env_int("PKV_CASCADE_TASK_CHUNKS", 8);
+  a.early_trigger = 0;
+  a.late_wait = late_wait;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
@@ -727,6 +764,162 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
 }
 
 }  // namespace
+
+namespace {
+
+// Shared-prefix decode: workspace layout and key splits.
+struct SharedPlan {
+  DecodePlan dec;
+  int32_t shared_len = 0, split_keys = 0, n_split = 0, item_tokens = 0;
+  int64_t grid_items = 0;
+  size_t off_meta = 0, off_lse = 0, off_plse = 0, off_po = 0, bytes = 0;
+};
+
+pkv_status plan_shared(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t prefix_blocks, SharedPlan* out) {
+  const pkv_pool_desc& d = p->desc;
+  if (d.dtype != PKV_BF16 || (d.head_dim != 64 && d.head_dim != 128) || d.block_size % pkv_dev::kChunk != 0)
+    return PKV_ERR_INVALID;
+  if (n_seqs <= 0 || Hq <= 0 || Hq % d.num_kv_heads != 0) return PKV_ERR_INVALID;
+  if (prefix_blocks <= 0 || prefix_blocks > d.max_blocks_per_seq) return PKV_ERR_INVALID;
+  const int g = Hq / d.num_kv_heads;
+  SharedPlan sp;
+  sp.item_tokens = tc_item_tokens(d.head_dim, g);
+  if (sp.item_tokens == 0) return PKV_ERR_INVALID;
+  const pkv_status st = plan_decode(p, n_seqs, Hq, 0, 1, &sp.dec, true);
+  if (st != PKV_OK) return st;
+  sp.shared_len = prefix_blocks * d.block_size;
+  // key splits of the shared prefix: about one work item per SM in all
+  const int64_t items_per_split = (static_cast<int64_t>(n_seqs) + sp.item_tokens - 1) / sp.item_tokens * d.num_kv_heads;
+  const int sms = num_sms();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  int64_t ns = (sms + items_per_split / 2) / items_per_split;
+  const int64_t max_split = (sp.shared_len + 63) / 64;
+  ns = ns < 1 ? 1 : (ns > max_split ? max_split : ns);
+  sp.split_keys = static_cast<int32_t>(((sp.shared_len + ns - 1) / ns + 63) / 64 * 64);
+  const int forced = env_int("PKV_SHARED_SPLIT_KEYS", 0);   // tuning: keys per split (multiple of 64)
+  if (forced >= 64 && forced % 64 == 0) sp.split_keys = forced;
+  sp.n_split = (sp.shared_len + sp.split_keys - 1) / sp.split_keys;
+  sp.grid_items = items_per_split * sp.n_split;
+  const size_t rows = static_cast<size_t>(n_seqs) * Hq;
+  sp.off_meta = round_up(sp.dec.ws_bytes, 256);
+  sp.off_lse = sp.off_meta + round_up((static_cast<size_t>(n_seqs) + 2) * sizeof(int32_t), 256);
+  sp.off_plse = sp.off_lse + round_up(rows * sizeof(float), 256);
+  sp.off_po = sp.off_plse + round_up(static_cast<size_t>(sp.n_split) * rows * sizeof(float), 256);
+  sp.bytes = sp.off_po + static_cast<size_t>(sp.n_split) * rows * d.head_dim * sizeof(float);
+  *out = sp;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_decode_shared_prefix_workspace_bytes(const pkv_pool* p, int32_t n_seqs, int32_t num_q_heads,
+                                                int32_t prefix_blocks) {
+  if (!p) return 0;
+  if (prefix_blocks == 0) return pkv_decode_workspace_bytes(p, n_seqs, num_q_heads, 0);
+  SharedPlan sp;
+  if (plan_shared(p, n_seqs, num_q_heads, prefix_blocks, &sp) != PKV_OK) return 0;
+  return sp.bytes;
+}
+
+pkv_status pkv_paged_decode_shared_prefix(const pkv_pool* p, float* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads,
+                                          float scale, int32_t prefix_blocks, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  if (!p || n_seqs < 0 || prefix_blocks < 0) return PKV_ERR_INVALID;
+  if (n_seqs == 0) return PKV_OK;
+  if (prefix_blocks == 0)
+    return pkv_paged_decode(p, out, q, k_cache, v_cache, block_tables, context_lens, n_seqs, num_q_heads, scale, 0,
+                            workspace, workspace_bytes, stream);
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace) return PKV_ERR_INVALID;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return PKV_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID;
+  SharedPlan sp;
+  const pkv_status st = plan_shared(p, n_seqs, num_q_heads, prefix_blocks, &sp);
+  if (st != PKV_OK) return st;
+  if (workspace_bytes < sp.bytes) return PKV_ERR_INVALID;
+  const pkv_pool_desc& d = p->desc;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  float* lse_s = reinterpret_cast<float*>(ws + sp.off_lse);
+  float* part_lse = reinterpret_cast<float*>(ws + sp.off_plse);
+  float* part_o = reinterpret_cast<float*>(ws + sp.off_po);
+  int32_t* meta = reinterpret_cast<int32_t*>(ws + sp.off_meta);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // 1. the shared prefix once for every row: tensor-core kernel in shared-prefix mode, key splits.
+  // Once past its own dependency wait it lets the decode launch: decode CTAs take the SMs it leaves
+  // free and, by dynamic tasks, the rest as its CTAs finish.
+  pkv_dev::PrefillArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.out = nullptr;
+  a.q = q;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.cu_q = nullptr;
+  a.n_seqs = 1;
+  a.Hq = num_q_heads;
+  a.Hkv = d.num_kv_heads;
+  a.B = d.block_size;
+  a.NB = d.num_blocks;
+  a.MB = d.max_blocks_per_seq;
+  a.window = 0;
+  a.stages = 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = p->d_err_word;
+  a.total_q = n_seqs;
+  a.shared_len = sp.shared_len;
+  a.split_keys = sp.split_keys;
+  a.part_o = part_o;
+  a.part_lse = part_lse;
+  a.early_trigger = 1;
+  const unsigned long long tag = next_call_tag();   // the decode's call tag, installed by this kernel
+  a.task_ctr = reinterpret_cast<unsigned long long*>(ws);
+  a.task_tag = tag;
+  pkv_status r = tc_prefill_launch(p, a, k_cache, v_cache, s, sp.grid_items);
+  if (r != PKV_OK) return r;
+  // 2. private suffixes: decode over positions [shared_len, len) with each row's log-sum-exp, in
+  // deferred-merge mode (dynamic tasks; units cut by task boundaries leave partials for step 3). It
+  // reads nothing step 1 writes; it waits for step 1 only before it completes, so that step 3 (which
+  // waits for it) sees both.
+  r = decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs, num_q_heads,
+                    scale, 0, 0, workspace, sp.dec.ws_bytes, stream, sp.shared_len, lse_s, meta, 1, tag);
+  if (r != PKV_OK) return r;
+  // 3. log-sum-exp merge of every row's parts: suffix (final row or split-unit partials) and prefix splits
+  pkv_dev::CascadeMergeArgs m;
+  m.out = out;
+  m.lse_s = lse_s;
+  m.part_o = part_o;
+  m.part_lse = part_lse;
+  m.dec_o = reinterpret_cast<const float*>(ws + sp.dec.off_o);
+  m.dec_ml = reinterpret_cast<const float*>(ws + sp.dec.off_ml);
+  m.meta = meta;
+  m.task_ctr = reinterpret_cast<unsigned long long*>(ws);   // the decode's first workspace word
+  m.tables = block_tables;
+  m.n_rows = static_cast<int64_t>(n_seqs) * num_q_heads;
+  m.D = d.head_dim;
+  m.G = num_q_heads / d.num_kv_heads;
+  m.Hkv = d.num_kv_heads;
+  m.n_split = sp.n_split;
+  m.MB = d.max_blocks_per_seq;
+  m.n_seqs = n_seqs;
+  m.prefix_blocks = prefix_blocks;
+  m.err = p->d_err_word;
+  // one wave: a warp per row, rows beyond the resident warps taken grid-stride
+  const int per_sm = occupancy(reinterpret_cast<const void*>(pkv_dev::merge_prefix_kernel), 256, 0);
+  const int64_t wave = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * num_sms();
+  const int64_t want = (m.n_rows + 7) / 8;
+  const int64_t blocks = want < wave ? want : wave;
+  if (launch(pkv_dev::merge_prefix_kernel, dim3(static_cast<unsigned>(blocks > 0 ? blocks : 1)), dim3(256), 0, s,
+             m) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // extern "C"
 
 extern "C" {
 

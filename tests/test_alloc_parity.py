@@ -115,6 +115,33 @@ def test_prefix_workload_trace():
                 a, b = lib.alloc_raw(s, op[2]), m.alloc(s, op[2])
                 assert a[0] == b[0] == 0 and a[2].tolist() == b[2] and a[3] == b[3]
         same_state(lib, m)
+        # sharing structure: the prompt's full blocks, shared by all children (closed form), and the
+        # brute-force count over the model's tables
+        kids = [ids[i] for i in range(len(ids))]
+        assert lib.shared_prefix_blocks(kids) == w.length_args[0] // w.block_size
+        mt, ml = m.block_table(kids)
+        k = 0
+        while k < min(ml) // w.block_size and len({row[k] for row in mt}) == 1:
+            k += 1
+        assert lib.shared_prefix_blocks(kids) == k
+        assert lib.shared_prefix_blocks(kids[:1]) == ml[0] // w.block_size
+
+
+def test_shared_prefix_blocks_hand_worked():
+    """Block 4: a 10-token prompt (2 full blocks + 2 tokens), two forks; child 0 appends 7 tokens (its
+    first append copies the partial block), child 1 appends nothing. Shared full blocks: 2. Child 1
+    alone: 10 // 4 = 2 full blocks. A fresh unrelated sequence shares none."""
+    lib = pkv.Pool(1, 1, 8, 4, 32, 8, 8, pkv.BF16)
+    root, _, _ = lib.alloc(-1, 10)
+    c0, c1 = lib.fork(root), lib.fork(root)
+    lib.alloc(c0, 7)
+    assert lib.shared_prefix_blocks([c0, c1]) == 2
+    assert lib.shared_prefix_blocks([c1]) == 2
+    assert lib.shared_prefix_blocks([c0]) == 17 // 4
+    other, _, _ = lib.alloc(-1, 12)
+    assert lib.shared_prefix_blocks([c0, other]) == 0
+    with pytest.raises(pkv.PagedKVError):
+        lib.shared_prefix_blocks([])
 
 
 def test_large_pool_constructs_fast():
