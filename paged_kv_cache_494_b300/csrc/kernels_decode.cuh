@@ -1004,23 +1004,56 @@ struct Fp8Math {
 };
 
 
-// Tasks of a deferred-mode decode: about NP / min_chunks, each more than S chunks (the producer then
-// runs at most one task ahead of the consumer), at most max_tasks.
-__device__ __forceinline__ int64_t defer_task_count(int64_t NP, int32_t min_chunks, int S, int32_t max_tasks) {
-  const int64_t tc = min_chunks > S + 1 ? min_chunks : S + 1;
-  const int64_t T = NP / tc;
-  return T < 1 ? 1 : (T > max_tasks ? max_tasks : T);
+// Tasks of a deferred-mode decode, at fixed boundaries: the first 3/4 of the NP chunks in tasks of
+// about `big` = max(min_chunks, S + 1) chunks, the last quarter in tasks of about big / 4 (at least
+// S + 1: the producer then runs at most one task ahead of the consumer), at most max_tasks in all.
+// Warps take them in order, so the small ones fill the end, where warps finish at different times.
+struct TaskMap {
+  int64_t NP, NP1, T1, T2;   // chunks, chunks in the big tasks, big tasks, small tasks
+  __device__ __forceinline__ int64_t count() const { return T1 + T2; }
+  __device__ __forceinline__ int64_t lo(int64_t t) const {   // first chunk of task t (t <= T1 + T2)
+    if (t < T1) return NP1 * t / T1;
+    if (t >= T1 + T2) return NP;   // (one region: T2 = 0, NP1 = NP)
+    return NP1 + (NP - NP1) * (t - T1) / T2;
+  }
+  __device__ __forceinline__ int64_t of(int64_t p) const {   // task holding chunk p < NP
+    return p < NP1 ? ((p + 1) * T1 - 1) / NP1 : T1 + ((p - NP1 + 1) * T2 - 1) / (NP - NP1);
+  }
+};
+
+__device__ __forceinline__ TaskMap defer_task_map(int64_t NP, int32_t min_chunks, int S, int32_t max_tasks) {
+  TaskMap m;
+  m.NP = NP;
+  const int64_t big = min_chunks > S + 1 ? min_chunks : S + 1;
+  const int64_t small = big / 4 > S + 1 ? big / 4 : S + 1;
+  if (NP < 4 * big || max_tasks < 2) {   // one region
+    m.NP1 = NP;
+    m.T1 = NP / big < 1 ? 1 : (NP / big > max_tasks ? max_tasks : NP / big);
+    m.T2 = 0;
+    return m;
+  }
+  m.NP1 = NP * 3 / 4;
+  m.T1 = m.NP1 / big;
+  m.T2 = (NP - m.NP1) / small;
+  if (m.T1 + m.T2 > max_tasks) {   // keep the proportions within the slot budget (fewer, longer tasks)
+    const int64_t t1 = m.T1 * max_tasks / (m.T1 + m.T2);
+    const int64_t t2 = max_tasks - (t1 < 1 ? 1 : t1);
+    m.T1 = t1 < 1 ? 1 : t1;
+    m.T2 = t2 < 1 ? 1 : (t2 < m.T2 ? t2 : m.T2);
+  }
+  return m;
 }
 
 // ------------------------------------------------------------------------------------------------
 // Deferred-merge decode of one warp (balanced mode, defer_meta set): dynamic tasks, no merging.
-// The flat chunk list (NP chunks) is cut into T tasks at fixed boundaries NP t / T, so the segments
+// The flat chunk list (NP chunks) is cut into T tasks at fixed boundaries (TaskMap), so the segments
 // of a task, and their slots 2 t (the task's first segment) and 2 t + 1 (its last), do not depend on
 // which warp runs it. Every task is taken from the call's counter (a CTA's first tasks, one per
 // warp, by one atomic), so CTAs that start late (their SM was still busy) or warps that get slower
-// memory service take fewer, and CTAs that start after the last task was taken do nothing. A unit that one task holds whole is final: its rows go to `out` (and
-// lse_out). Every other segment leaves its partial in its slot for the kernel that follows, which
-// finds them from [T, pref[0..n]] (written here by block 0). The producer runs on into the next
+// memory service take fewer, and CTAs that start after the last task was taken do nothing.
+// [T1, T2, NP1 (low, high 32 bits), pref[0..n]] in defer_meta (block 0) give the merging kernel the
+// task boundaries. A unit that one task holds whole is final: its rows go to `out` (and
+// lse_out). Every other segment leaves its partial in its slot for the kernel that follows. The producer runs on into the next
 // task without draining the ring: tasks hold more than S chunks, so it is at most one task ahead.
 // ------------------------------------------------------------------------------------------------
 template <class Math, int D, int G>
@@ -1030,9 +1063,10 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
   constexpr int SB = Math::kStageBytes;
   const int S = a.stages;
   const int32_t n = a.n_seqs, Hkv = a.Hkv;
-  const int64_t T = defer_task_count(NP, a.min_chunks, S, a.max_tasks);
+  const TaskMap tm = defer_task_map(NP, a.min_chunks, S, a.max_tasks);
+  const int64_t T = tm.count();
   if (NP == 0) return;
-  auto t_lo = [&](int64_t t) { return NP * t / T; };
+  auto t_lo = [&](int64_t t) { return tm.lo(t); };
   auto next_task = [&]() -> int64_t {
     long long t = 0;
     if (lane == 0) t = grab_tasks(a.ws_count, a.tag, 1u, T);
@@ -1040,6 +1074,14 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
   };
   int64_t ctk = first_task;   // the consumer's task
   if (ctk >= T) return;
+  auto bad_range = [&](int64_t t) {   // a task's chunks lie in [0, NP) and are not empty
+    const int64_t l0 = t_lo(t), l1 = t_lo(t + 1);
+    return l0 < 0 || l1 > NP || l1 <= l0;
+  };
+  if (bad_range(ctk)) {
+    record_error(ERRBIT_BOUNDS);
+    return;
+  }
 
   // --- producer: (p_pg, p_sub) = page and chunk within the page of pf; ntk = task after ctk ---
   const int32_t cpb = a.B / kChunk;
@@ -1095,6 +1137,10 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
       }
     } else {   // this task is issued: take the next one (the consumer's next task)
       ntk = next_task();
+      if (ntk < T && bad_range(ntk)) {
+        if (lane == 0) record_error(ERRBIT_BOUNDS);
+        ntk = T;
+      }
       if (ntk < T) {
         pf = locate(pref, n, Hkv, t_lo(ntk));
         p_left = t_lo(ntk + 1) - t_lo(ntk);
@@ -1209,6 +1255,10 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   set_error_word(a.err);
   if (!a.late_wait) pdl_wait();
   if (a.early_trigger) pdl_launch_dependents();
+  // deferred mode: the CTA's first tasks, one per warp, taken at once, while the prefix is built
+  // (wsum[8] is not used by the prefix build)
+  if (a.defer_meta != nullptr && threadIdx.x == 0)
+    wsum[8] = static_cast<int32_t>(grab_tasks(a.ws_count, a.tag, static_cast<unsigned int>(NW), 0x7fffffff));
   build_prefix(a, pref, ipref, cfirst, wsum);
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
@@ -1237,17 +1287,16 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   const int64_t Wmax = NP / mc > 0 ? NP / mc : 1;
   const int64_t Weff = Wmax < W ? Wmax : W;
   if (a.defer_meta != nullptr) {
-    const int64_t T = defer_task_count(NP, a.min_chunks, S, a.max_tasks);
+    const TaskMap tm = defer_task_map(NP, a.min_chunks, S, a.max_tasks);
     if (blockIdx.x == 0) {   // where the merging kernel finds each unit's parts
-      for (int32_t i = threadIdx.x; i <= n; i += blockDim.x) a.defer_meta[1 + i] = pref[i];
-      if (threadIdx.x == 0) a.defer_meta[0] = static_cast<int32_t>(T);
+      for (int32_t i = threadIdx.x; i <= n; i += blockDim.x) a.defer_meta[4 + i] = pref[i];
+      if (threadIdx.x == 0) {
+        a.defer_meta[0] = static_cast<int32_t>(tm.T1);
+        a.defer_meta[1] = static_cast<int32_t>(tm.T2);
+        a.defer_meta[2] = static_cast<int32_t>(tm.NP1 & 0xffffffffll);
+        a.defer_meta[3] = static_cast<int32_t>(tm.NP1 >> 32);
+      }
     }
-    // the CTA's first tasks, one per warp, in one atomic (wsum[8] is free after the prefix build)
-    if (threadIdx.x == 0) {
-      const int64_t t0 = NP > 0 ? grab_tasks(a.ws_count, a.tag, static_cast<unsigned int>(NW), T) : T;
-      wsum[8] = static_cast<int32_t>(t0 < T ? t0 : T);
-    }
-    __syncthreads();
     decode_deferred<Math, D, G>(a, maps, ring, bars, pref, cfirst, NP, static_cast<int64_t>(wsum[8]) + warp, lane);
     if (a.late_wait) pdl_wait();
     pdl_launch_dependents();
@@ -1530,7 +1579,7 @@ struct CascadeMergeArgs {
   const float* part_lse;    // [n_split][n_rows]
   const float* dec_o;       // decode slots [2 W][G][D] (normalised)
   const float* dec_ml;      // decode slots [2 W][G][2] (m, l)
-  const int32_t* meta;      // [T, pref[0..n]] written by the decode
+  const int32_t* meta;      // [T1, T2, NP1 low, NP1 high, pref[0..n]] written by the decode
   unsigned long long* task_ctr;   // the decode's task counter: zeroed here (CUDA-graph replays reuse the call tag)
   const int32_t* tables;
   int64_t n_rows;
@@ -1551,23 +1600,26 @@ __global__ void __launch_bounds__(256, 4) merge_prefix_kernel(const __grid_const
   const int lane = threadIdx.x & 31;
   const int D = a.D, Hq = a.Hkv * a.G;
   const bool has_c = lane < D / 4;                 // this lane's float4 of the row
-  const int64_t T = __ldg(a.meta);   // the decode's task count
-  const int32_t* pref = a.meta + 1;
-  const int64_t NP = static_cast<int64_t>(__ldg(pref + a.n_seqs)) * a.Hkv;
+  const int32_t* pref = a.meta + 4;
+  TaskMap tm;   // the decode's task boundaries
+  tm.NP = static_cast<int64_t>(__ldg(pref + a.n_seqs)) * a.Hkv;
+  tm.T1 = __ldg(a.meta);
+  tm.T2 = __ldg(a.meta + 1);
+  tm.NP1 = static_cast<int64_t>(static_cast<uint32_t>(__ldg(a.meta + 2))) | (static_cast<int64_t>(__ldg(a.meta + 3)) << 32);
   constexpr int kBatch = 4;
   for (int64_t row = gtid >> 5; row < a.n_rows; row += gthreads >> 5) {
     const int32_t b = static_cast<int32_t>(row / Hq), j = static_cast<int32_t>(row - static_cast<int64_t>(b) * Hq);
     const int32_t h = j / a.G, jj = j - h * a.G;
     // the suffix parts of the row: none (empty suffix), the final row (unit of one task), or one
-    // partial per task of a cut unit (task boundaries NP t / T: task_of(p) = floor(((p + 1) T - 1) / NP))
+    // partial per task of a cut unit
     const int64_t nch = __ldg(pref + b + 1) - __ldg(pref + b);
     int64_t wf = 0, n_suf = 0;
     int first_kind = 0;
     if (nch > 0) {
       const int64_t s_u = static_cast<int64_t>(__ldg(pref + b)) * a.Hkv + h * nch, e_u = s_u + nch;
-      wf = ((s_u + 1) * T - 1) / NP;
-      n_suf = (e_u * T - 1) / NP - wf + 1;
-      first_kind = (s_u == NP * wf / T) ? 0 : 1;
+      wf = tm.of(s_u);
+      n_suf = tm.of(e_u - 1) - wf + 1;
+      first_kind = (s_u == tm.lo(wf)) ? 0 : 1;
     }
     const bool whole = n_suf == 1;
     const int64_t n_parts = (n_suf > 1 ? n_suf : 0) + a.n_split;

@@ -244,11 +244,8 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
 
   set_error_word(a.err);
   pdl_wait();   // before any global access, and before holding tensor memory
-  if (a.task_ctr != nullptr && blockIdx.x == 0 && tid == 0) {
-    install_task_tag(a.task_ctr, a.task_tag);
-    __threadfence();
-  }
   if (a.early_trigger) pdl_launch_dependents();
+  if (a.task_ctr != nullptr && blockIdx.x == 0 && tid == 0) install_task_tag(a.task_ctr, a.task_tag);
 
   // ---- items per sequence (prefix over sequences) and the largest count; shared-prefix mode: one
   // virtual sequence whose queries are all total_q rows

@@ -753,7 +753,7 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   a.defer_meta = defer ? defer_meta : nullptr;
   a.max_tasks = pl.max_tasks;
   // deferred mode: chunks per task (no arrivals, so cutting units costs no fences; small tasks balance)
-  if (defer) a.min_chunks = env_int("PKV_CASCADE_TASK_CHUNKS", 8);
+  if (defer) a.min_chunks = env_int("PKV_CASCADE_TASK_CHUNKS", 16);
   a.early_trigger = 0;
   a.late_wait = late_wait;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -788,11 +788,15 @@ pkv_status plan_shared(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pr
   const pkv_status st = plan_decode(p, n_seqs, Hq, 0, 1, &sp.dec, true);
   if (st != PKV_OK) return st;
   sp.shared_len = prefix_blocks * d.block_size;
-  // key splits of the shared prefix: about one work item per SM in all
+  // key splits of the shared prefix: work items for about a quarter of the SMs. The tensor-core
+  // kernel runs beside the suffix decode, and each SM it holds is one the decode cannot stream on
+  // (its copies in flight are bounded by shared memory per SM); longer key ranges per item cost
+  // less than that (measured on 128 children of a 1,024-token prompt: 2 splits of 512 keys, 32 CTAs,
+  // against 8 splits of 128 keys, 128 CTAs).
   const int64_t items_per_split = (static_cast<int64_t>(n_seqs) + sp.item_tokens - 1) / sp.item_tokens * d.num_kv_heads;
   const int sms = num_sms();
   if (sms <= 0) return PKV_ERR_CUDA;
-  int64_t ns = (sms + items_per_split / 2) / items_per_split;
+  int64_t ns = (sms / 4 + items_per_split / 2) / items_per_split;
   const int64_t max_split = (sp.shared_len + 63) / 64;
   ns = ns < 1 ? 1 : (ns > max_split ? max_split : ns);
   sp.split_keys = static_cast<int32_t>(((sp.shared_len + ns - 1) / ns + 63) / 64 * 64);
@@ -802,7 +806,7 @@ pkv_status plan_shared(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pr
   sp.grid_items = items_per_split * sp.n_split;
   const size_t rows = static_cast<size_t>(n_seqs) * Hq;
   sp.off_meta = round_up(sp.dec.ws_bytes, 256);
-  sp.off_lse = sp.off_meta + round_up((static_cast<size_t>(n_seqs) + 2) * sizeof(int32_t), 256);
+  sp.off_lse = sp.off_meta + round_up((static_cast<size_t>(n_seqs) + 5) * sizeof(int32_t), 256);
   sp.off_plse = sp.off_lse + round_up(rows * sizeof(float), 256);
   sp.off_po = sp.off_plse + round_up(static_cast<size_t>(sp.n_split) * rows * sizeof(float), 256);
   sp.bytes = sp.off_po + static_cast<size_t>(sp.n_split) * rows * d.head_dim * sizeof(float);
