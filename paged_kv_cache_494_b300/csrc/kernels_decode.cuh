@@ -111,20 +111,21 @@ __device__ __forceinline__ bool arrive_last(unsigned long long* ctr, unsigned lo
 }
 
 // Take k consecutive dynamic tasks of a deferred-mode decode; returns the first index. The counter
-// holds (call tag << 16) | count. A value left by an earlier call (another tag, or fresh memory) is
-// replaced by this call's tag with count k by whichever taker gets there first, which takes index 0.
-// Returns `none` (and records PKV_ERR_DEVICE_TIMEOUT) if the counter could not be taken in a bounded
-// number of tries.
+// holds (low 32 bits of the call tag << 32) | count. A value left by an earlier call (another tag, or
+// fresh memory) is replaced by this call's tag with count k by whichever taker gets there first,
+// which takes index 0. Returns `none` (and records PKV_ERR_DEVICE_TIMEOUT) if the counter could not
+// be taken in a bounded number of tries.
 __device__ __forceinline__ int64_t grab_tasks(unsigned long long* ctr, unsigned long long tag, unsigned int k,
                                               int64_t none) {
+  const unsigned long long tg = tag & 0xffffffffull;   // odd, so never the zero of fresh memory
   unsigned long long cur = ld_relaxed_gpu(ctr);
   for (int it = 0; it < 256; ++it) {
-    if ((cur >> 16) == tag) {
+    if ((cur >> 32) == tg) {
       const unsigned long long v = atomicAdd(ctr, static_cast<unsigned long long>(k));
-      if ((v >> 16) == tag) return static_cast<int64_t>(v & 0xffffull);
-      cur = v + k;   // (cannot happen once installed: tags never go back)
+      if ((v >> 32) == tg) return static_cast<int64_t>(v & 0xffffffffull);
+      cur = v + k;   // (cannot happen once installed: the tag is only ever replaced by a later call)
     }
-    const unsigned long long prev = atomicCAS(ctr, cur, (tag << 16) | k);
+    const unsigned long long prev = atomicCAS(ctr, cur, (tg << 32) | k);
     if (prev == cur) return 0;
     cur = prev;
   }
@@ -1045,49 +1046,50 @@ __device__ __forceinline__ TaskMap defer_task_map(int64_t NP, int32_t min_chunks
 }
 
 // ------------------------------------------------------------------------------------------------
-// Deferred-merge decode of one warp (balanced mode, defer_meta set): dynamic tasks, no merging.
-// The flat chunk list (NP chunks) is cut into T tasks at fixed boundaries (TaskMap), so the segments
-// of a task, and their slots 2 t (the task's first segment) and 2 t + 1 (its last), do not depend on
-// which warp runs it. Every task is taken from the call's counter (a CTA's first tasks, one per
-// warp, by one atomic), so CTAs that start late (their SM was still busy) or warps that get slower
-// memory service take fewer, and CTAs that start after the last task was taken do nothing.
-// [T1, T2, NP1 (low, high 32 bits), pref[0..n]] in defer_meta (block 0) give the merging kernel the
-// task boundaries. A unit that one task holds whole is final: its rows go to `out` (and
-// lse_out). Every other segment leaves its partial in its slot for the kernel that follows. The producer runs on into the next
-// task without draining the ring: tasks hold more than S chunks, so it is at most one task ahead.
+// Deferred-merge decode of one warp (defer_meta set): dynamic tasks, no merging here.
+// Tasks have fixed chunk ranges, so a task's segments and their slots do not depend on which warp
+// runs it: in balanced mode the TaskMap boundaries (slots 2 t for the task's first segment, 2 t + 1
+// for its last), in fixed-partition mode one task per (unit, partition) item (slot u * max_parts + k,
+// as in the in-kernel merge). Every task is taken from the call's counter (a CTA's first tasks, one
+// per warp, by one atomic at kernel entry), so CTAs that start late (their SM was still busy) or
+// warps that get slower memory service take fewer, and CTAs that start after the last task was
+// taken do nothing. A unit one task holds whole is final: its rows go to `out` (and lse_out). Every
+// other segment leaves its partial in its slot for the merging kernel that follows, which finds
+// them from defer_meta (written by block 0). The producer runs on into the next task without
+// draining the ring and records each stage's task in stage_task, from which the consumer switches.
 // ------------------------------------------------------------------------------------------------
 template <class Math, int D, int G>
 __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMaps& maps, unsigned char* ring,
-                                                uint64_t* bars, const int32_t* pref, const int32_t* cfirst,
-                                                int64_t NP, int64_t first_task, int lane) {
+                                                uint64_t* bars, const int32_t* pref, const int32_t* ipref,
+                                                const int32_t* cfirst, int64_t NP, int64_t first_task,
+                                                int32_t* stage_task, int lane) {
   constexpr int SB = Math::kStageBytes;
   const int S = a.stages;
-  const int32_t n = a.n_seqs, Hkv = a.Hkv;
+  const int32_t n = a.n_seqs, Hkv = a.Hkv, PC = a.part_chunks;
   const TaskMap tm = defer_task_map(NP, a.min_chunks, S, a.max_tasks);
-  const int64_t T = tm.count();
+  const int64_t T = PC > 0 ? static_cast<int64_t>(ipref[n]) * Hkv : tm.count();
   if (NP == 0) return;
-  auto t_lo = [&](int64_t t) { return tm.lo(t); };
+  auto t_lo = [&](int64_t t) { return PC > 0 ? item_start(pref, ipref, n, Hkv, PC, t) : tm.lo(t); };
   auto next_task = [&]() -> int64_t {
     long long t = 0;
     if (lane == 0) t = grab_tasks(a.ws_count, a.tag, 1u, T);
     return __shfl_sync(0xffffffffu, t, 0);
   };
-  int64_t ctk = first_task;   // the consumer's task
-  if (ctk >= T) return;
   auto bad_range = [&](int64_t t) {   // a task's chunks lie in [0, NP) and are not empty
     const int64_t l0 = t_lo(t), l1 = t_lo(t + 1);
     return l0 < 0 || l1 > NP || l1 <= l0;
   };
-  if (bad_range(ctk)) {
-    record_error(ERRBIT_BOUNDS);
+  int64_t ptk = first_task;   // the producer's task
+  if (ptk >= T) return;
+  if (bad_range(ptk)) {
+    if (lane == 0) record_error(ERRBIT_BOUNDS);
     return;
   }
 
-  // --- producer: (p_pg, p_sub) = page and chunk within the page of pf; ntk = task after ctk ---
+  // --- producer: (p_pg, p_sub) = page and chunk within the page of pf ---
   const int32_t cpb = a.B / kChunk;
-  Cursor pf = locate(pref, n, Hkv, t_lo(ctk));
-  int64_t p_left = t_lo(ctk + 1) - t_lo(ctk);
-  int64_t ntk = T;
+  Cursor pf = locate(pref, n, Hkv, t_lo(ptk));
+  int64_t p_left = t_lo(ptk + 1) - t_lo(ptk);
   bool p_done = false;
   int32_t p_pg = 0, p_sub = 0;
   auto p_unit_start = [&]() {
@@ -1113,6 +1115,7 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
     }
     const int32_t blk = __shfl_sync(0xffffffffu, win_val, p_pg - win_base);
     if (lane == 0) {
+      stage_task[stage] = static_cast<int32_t>(ptk);
       const uint32_t bar = smem_addr(bars + stage);
       if (blk >= 0 && blk < a.NB) {
         const int64_t row0 = (static_cast<int64_t>(blk) * Hkv + pf.h) * a.B + p_sub * kChunk;
@@ -1135,15 +1138,15 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
         advance(pf, pref, n, Hkv);
         p_unit_start();
       }
-    } else {   // this task is issued: take the next one (the consumer's next task)
-      ntk = next_task();
-      if (ntk < T && bad_range(ntk)) {
+    } else {   // this task is issued: take the next one
+      ptk = next_task();
+      if (ptk < T && bad_range(ptk)) {
         if (lane == 0) record_error(ERRBIT_BOUNDS);
-        ntk = T;
+        ptk = T;
       }
-      if (ntk < T) {
-        pf = locate(pref, n, Hkv, t_lo(ntk));
-        p_left = t_lo(ntk + 1) - t_lo(ntk);
+      if (ptk < T) {
+        pf = locate(pref, n, Hkv, t_lo(ptk));
+        p_left = t_lo(ptk + 1) - t_lo(ptk);
         p_unit_start();
       } else {
         p_done = true;
@@ -1151,21 +1154,29 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
     }
   };
   for (int s = 0; s < S && !p_done; ++s) issue(s);
+  __syncwarp();
 
-  // --- consumer ---
-  Cursor cc = locate(pref, n, Hkv, t_lo(ctk));
-  int64_t c_left = t_lo(ctk + 1) - t_lo(ctk);
+  // --- consumer: switches task when the current one is used up (stage_task names the next) ---
+  int64_t ctk = -1, c_left = 0;
+  Cursor cc;
   typename Math::Regs r;
-  int32_t seg_c0 = cc.c;
+  int32_t seg_c0 = 0, len_b = 0;
   int seg_idx = 0;
   int stage = 0;
   uint32_t phase = 0;
-  int32_t len_b = clamped_len(a, cc.b);
-  Math::load_q(r, a, cc.b, cc.h, lane);
-  Math::reset(r);
   int64_t consumed = 0;
   bool aborted = false;
-  while (true) {
+  while (consumed < issued) {
+    if (c_left == 0) {   // the chunk at this stage begins the next task
+      ctk = stage_task[stage];
+      cc = locate(pref, n, Hkv, t_lo(ctk));
+      c_left = t_lo(ctk + 1) - t_lo(ctk);
+      seg_c0 = cc.c;
+      seg_idx = 0;
+      len_b = clamped_len(a, cc.b);
+      Math::load_q(r, a, cc.b, cc.h, lane);
+      Math::reset(r);
+    }
     if (!mbar_wait_bounded(smem_addr(bars + stage), phase)) {
       aborted = true;
       break;
@@ -1180,6 +1191,7 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
     __syncwarp();
     ++consumed;
     if (!p_done) issue(stage);
+    __syncwarp();   // stage_task written by lane 0 before any lane reads it
     if (++stage == S) {
       stage = 0;
       phase ^= 1u;
@@ -1191,7 +1203,8 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
         Math::finish(r, a.out + (static_cast<int64_t>(cc.b) * a.Hq + cc.h * G) * D, nullptr,
                      a.lse_out ? a.lse_out + static_cast<int64_t>(cc.b) * a.Hq + cc.h * G : nullptr, lane);
       } else {
-        const int64_t slot = 2 * ctk + (seg_idx == 0 ? 0 : 1);
+        const int64_t slot = PC > 0 ? (static_cast<int64_t>(cc.b) * Hkv + cc.h) * a.max_parts + cc.c / PC
+                                    : 2 * ctk + (seg_idx == 0 ? 0 : 1);
         Math::finish(r, a.ws_o + slot * G * D, a.ws_ml + slot * G * 2, nullptr, lane);
       }
       ++seg_idx;
@@ -1205,16 +1218,6 @@ __device__ __forceinline__ void decode_deferred(const DecodeArgs& a, const TmaMa
         Math::reset(r);
         seg_c0 = cc.c;
       }
-    } else {
-      if (ntk >= T) break;   // the producer found no task after this one
-      ctk = ntk;
-      cc = locate(pref, n, Hkv, t_lo(ctk));
-      c_left = t_lo(ctk + 1) - t_lo(ctk);
-      seg_c0 = cc.c;
-      seg_idx = 0;
-      len_b = clamped_len(a, cc.b);
-      Math::load_q(r, a, cc.b, cc.h, lane);
-      Math::reset(r);
     }
   }
   if (aborted) {   // drain the copies still in flight, each with one more bounded wait
@@ -1289,15 +1292,21 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   if (a.defer_meta != nullptr) {
     const TaskMap tm = defer_task_map(NP, a.min_chunks, S, a.max_tasks);
     if (blockIdx.x == 0) {   // where the merging kernel finds each unit's parts
-      for (int32_t i = threadIdx.x; i <= n; i += blockDim.x) a.defer_meta[4 + i] = pref[i];
+      for (int32_t i = threadIdx.x; i <= n; i += blockDim.x) {
+        a.defer_meta[5 + i] = pref[i];
+        if (PC > 0) a.defer_meta[5 + (n + 1) + i] = ipref[i];
+      }
       if (threadIdx.x == 0) {
-        a.defer_meta[0] = static_cast<int32_t>(tm.T1);
-        a.defer_meta[1] = static_cast<int32_t>(tm.T2);
-        a.defer_meta[2] = static_cast<int32_t>(tm.NP1 & 0xffffffffll);
-        a.defer_meta[3] = static_cast<int32_t>(tm.NP1 >> 32);
+        a.defer_meta[0] = PC;
+        a.defer_meta[1] = static_cast<int32_t>(tm.T1);
+        a.defer_meta[2] = static_cast<int32_t>(tm.T2);
+        a.defer_meta[3] = static_cast<int32_t>(tm.NP1 & 0xffffffffll);
+        a.defer_meta[4] = static_cast<int32_t>(tm.NP1 >> 32);
       }
     }
-    decode_deferred<Math, D, G>(a, maps, ring, bars, pref, cfirst, NP, static_cast<int64_t>(wsum[8]) + warp, lane);
+    // stage_task of this warp: wsum[40 + 4 warp + stage] (S <= 4; not used by the prefix build)
+    decode_deferred<Math, D, G>(a, maps, ring, bars, pref, ipref, cfirst, NP, static_cast<int64_t>(wsum[8]) + warp,
+                                wsum + 40 + 4 * warp, lane);
     if (a.late_wait) pdl_wait();
     pdl_launch_dependents();
     return;
@@ -1560,18 +1569,18 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   }
 }
 
-// Shared-prefix (cascade) merge. A batch whose sequences all begin with the same prefix_blocks
-// physical blocks is attended in two parts: each sequence's private suffix by the decode kernel in
-// deferred-merge mode (rows of units that one warp finished are final in `out` with their log-sum-exp
-// lse_s; units split over warps left one partial per warp in the decode workspace), and the shared
-// prefix once for all rows by the tensor-core prefill kernel in shared-prefix mode (n_split key
-// splits, part_o / part_lse). The exact attention over the whole context is the log-sum-exp
-// combination of all those parts ("Servicio de modelos de lenguaje con un presupuesto de memoria" §6:
+// Merge after a deferred-mode decode. The decode left, for each (sequence, KV head) unit, either the
+// final rows in `out` (with their log-sum-exp in lse_s when one is wanted: a unit one task held
+// whole) or one normalised partial per task of a unit cut by task boundaries. For a shared-prefix
+// (cascade) call the decode covered only each sequence's private suffix, and the tensor-core prefill
+// kernel in shared-prefix mode attended the shared prefix once for all rows (n_split key splits,
+// part_o / part_lse). The exact attention over the whole context is the log-sum-exp combination of
+// all of a row's parts ("Servicio de modelos de lenguaje con un presupuesto de memoria" §6:
 // blockwise exact attention with running statistics):
 //     M = max_k lse_k, w_k = 2^(lse_k - M), out = sum_k w_k o_k / sum_k w_k   (each o_k normalised).
-// One warp per (sequence, query head) row, the loads of 4 parts in flight at a time. The kernel also
-// checks that every table of the call begins with sequence 0's first prefix_blocks entries (else
-// PKV_ERR_DEVICE_BOUNDS).
+// One warp per (sequence, query head) row, the loads of 4 parts in flight at a time; a final row
+// with no prefix parts is left as it is. With prefix_blocks > 0 the kernel also checks that every
+// table of the call begins with sequence 0's first prefix_blocks entries (else PKV_ERR_DEVICE_BOUNDS).
 struct CascadeMergeArgs {
   float* out;
   const float* lse_s;       // [n_rows] suffix log-sum-exp of rows whose unit was not split
@@ -1579,7 +1588,8 @@ struct CascadeMergeArgs {
   const float* part_lse;    // [n_split][n_rows]
   const float* dec_o;       // decode slots [2 W][G][D] (normalised)
   const float* dec_ml;      // decode slots [2 W][G][2] (m, l)
-  const int32_t* meta;      // [T1, T2, NP1 low, NP1 high, pref[0..n]] written by the decode
+  const int32_t* meta;      // [part_chunks, T1, T2, NP1 low, NP1 high, pref[0..n], ipref[0..n] (partitions)]
+  int32_t max_parts;        // fixed-partition mode: slots per unit
   unsigned long long* task_ctr;   // the decode's task counter: zeroed here (CUDA-graph replays reuse the call tag)
   const int32_t* tables;
   int64_t n_rows;
@@ -1592,7 +1602,7 @@ __global__ void __launch_bounds__(256, 4) merge_prefix_kernel(const __grid_const
   pdl_wait();
   const int64_t gthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (gtid == 0) *a.task_ctr = 0ull;   // the decode has completed: every task was taken
+  if (gtid == 0 && a.task_ctr != nullptr) *a.task_ctr = 0ull;   // the decode has completed
   for (int64_t i = gtid; i < static_cast<int64_t>(a.n_seqs) * a.prefix_blocks; i += gthreads) {
     const int64_t b = i / a.prefix_blocks, k = i - b * a.prefix_blocks;
     if (__ldg(a.tables + b * a.MB + k) != __ldg(a.tables + k)) record_error(ERRBIT_BOUNDS);
@@ -1600,12 +1610,13 @@ __global__ void __launch_bounds__(256, 4) merge_prefix_kernel(const __grid_const
   const int lane = threadIdx.x & 31;
   const int D = a.D, Hq = a.Hkv * a.G;
   const bool has_c = lane < D / 4;                 // this lane's float4 of the row
-  const int32_t* pref = a.meta + 4;
-  TaskMap tm;   // the decode's task boundaries
+  const int32_t PC = __ldg(a.meta);
+  const int32_t* pref = a.meta + 5;
+  TaskMap tm;   // the decode's task boundaries (balanced mode)
   tm.NP = static_cast<int64_t>(__ldg(pref + a.n_seqs)) * a.Hkv;
-  tm.T1 = __ldg(a.meta);
-  tm.T2 = __ldg(a.meta + 1);
-  tm.NP1 = static_cast<int64_t>(static_cast<uint32_t>(__ldg(a.meta + 2))) | (static_cast<int64_t>(__ldg(a.meta + 3)) << 32);
+  tm.T1 = __ldg(a.meta + 1);
+  tm.T2 = __ldg(a.meta + 2);
+  tm.NP1 = static_cast<int64_t>(static_cast<uint32_t>(__ldg(a.meta + 3))) | (static_cast<int64_t>(__ldg(a.meta + 4)) << 32);
   constexpr int kBatch = 4;
   for (int64_t row = gtid >> 5; row < a.n_rows; row += gthreads >> 5) {
     const int32_t b = static_cast<int32_t>(row / Hq), j = static_cast<int32_t>(row - static_cast<int64_t>(b) * Hq);
@@ -1615,7 +1626,9 @@ __global__ void __launch_bounds__(256, 4) merge_prefix_kernel(const __grid_const
     const int64_t nch = __ldg(pref + b + 1) - __ldg(pref + b);
     int64_t wf = 0, n_suf = 0;
     int first_kind = 0;
-    if (nch > 0) {
+    if (nch > 0 && PC > 0) {   // fixed partitions: one task per partition, slot u * max_parts + k
+      n_suf = (nch + PC - 1) / PC;
+    } else if (nch > 0) {      // balanced: the tasks holding the unit's first and last chunks
       const int64_t s_u = static_cast<int64_t>(__ldg(pref + b)) * a.Hkv + h * nch, e_u = s_u + nch;
       wf = tm.of(s_u);
       n_suf = tm.of(e_u - 1) - wf + 1;
@@ -1623,10 +1636,15 @@ __global__ void __launch_bounds__(256, 4) merge_prefix_kernel(const __grid_const
     }
     const bool whole = n_suf == 1;
     const int64_t n_parts = (n_suf > 1 ? n_suf : 0) + a.n_split;
-    // part p < n_suf: decode slot of the split unit's p-th segment; then the prefix splits
+    if ((whole || n_parts == 0) && a.n_split == 0) continue;   // final already (or an empty row's zeros)
+    const int64_t u = static_cast<int64_t>(b) * a.Hkv + h;
+    auto slot_of = [&](int64_t p) -> int64_t {
+      return PC > 0 ? u * a.max_parts + p : 2 * (wf + p) + (p == 0 ? first_kind : 0);
+    };
+    // part p < n_suf: decode slot of the cut unit's p-th segment; then the prefix splits
     auto part_lse = [&](int64_t p) -> float {
       if (p < n_parts - a.n_split) {
-        const int64_t slot = 2 * (wf + p) + (p == 0 ? first_kind : 0);
+        const int64_t slot = slot_of(p);
         const float2 ml = __ldg(reinterpret_cast<const float2*>(a.dec_ml) + slot * a.G + jj);
         return ml.x + log2f(ml.y);
       }
@@ -1634,7 +1652,7 @@ __global__ void __launch_bounds__(256, 4) merge_prefix_kernel(const __grid_const
     };
     auto part_o = [&](int64_t p) -> const float4* {
       if (p < n_parts - a.n_split) {
-        const int64_t slot = 2 * (wf + p) + (p == 0 ? first_kind : 0);
+        const int64_t slot = slot_of(p);
         return reinterpret_cast<const float4*>(a.dec_o + (slot * a.G + jj) * D);
       }
       return reinterpret_cast<const float4*>(a.part_o + ((p - (n_parts - a.n_split)) * a.n_rows + row) * D);

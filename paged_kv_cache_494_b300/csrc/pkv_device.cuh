@@ -30,14 +30,16 @@ __device__ __forceinline__ void record_error(unsigned int bit) {
   atomicOr(w ? w : &g_error_bits, bit);
 }
 
-// Makes a tagged task counter ((tag << 16) | count) belong to this call: a value with another tag (an
-// earlier call's, or fresh memory) is replaced by (tag << 16) | 0; a value with this tag is left as it
+// Makes a tagged task counter ((low 32 bits of the tag) << 32 | count) belong to this call: a value
+// with another tag (an
+// earlier call's, or fresh memory) is replaced by (tag << 32) | 0; a value with this tag is left as it
 // is (takers may already have counted on it). Bounded: gives up quietly, and takers then install the
 // tag themselves.
 __device__ __forceinline__ void install_task_tag(unsigned long long* ctr, unsigned long long tag) {
+  const unsigned long long tg = tag & 0xffffffffull;
   unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
-  for (int it = 0; it < 64 && (cur >> 16) != tag; ++it) {
-    const unsigned long long prev = atomicCAS(ctr, cur, tag << 16);
+  for (int it = 0; it < 64 && (cur >> 32) != tg; ++it) {
+    const unsigned long long prev = atomicCAS(ctr, cur, tg << 32);
     if (prev == cur) return;
     cur = prev;
   }

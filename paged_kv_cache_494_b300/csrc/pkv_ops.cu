@@ -369,8 +369,17 @@ struct DecodePlan {
   size_t smem = 0;
   int part_chunks = 0, max_parts = 0;
   int64_t n_units = 0, n_slots = 0;
-  size_t off_ml = 0, off_o = 0, ws_bytes = 0;
+  size_t off_ml = 0, off_o = 0, off_meta = 0, ws_bytes = 0;
+  bool defer = false;
 };
+
+// Deferred-merge decode (dynamic tasks, then the merge kernel) for pkv_paged_decode(_window, _fp8)
+// when PKV_DECODE_DEFER=1; otherwise the in-kernel merge. Measured on B300 the deferred form is the
+// slower one for a whole batch (every task pays its own setup: locate, length and query loads, which a
+// static range pays once per unit): serving batch 0.826 against 0.868 of the copy bandwidth, 8 x 32k
+// tokens 217 / 248 us (512-token partitions / balanced) against 209 / 210 us. The shared-prefix decode
+// always uses it, since its merge kernel runs anyway and its decode starts beside another kernel.
+bool decode_defer_wanted(int32_t) { return env_int("PKV_DECODE_DEFER", 0) > 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -430,10 +439,8 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
     const int64_t max_chunks = (static_cast<int64_t>(d.max_blocks_per_seq) * d.block_size) / pkv_dev::kChunk;
     pl.max_parts = static_cast<int>((max_chunks + pl.part_chunks - 1) / pl.part_chunks);
     pl.n_slots = pl.n_units * pl.max_parts;
-  } else if (defer) {
-    // 16-bit task counts: tasks plus one CTA grab and one final grab per warp stay below 2^16
-    pl.max_tasks = 4 * pl.warps < 60000 - 2 * pl.warps ? 4 * pl.warps : 60000 - 2 * pl.warps;
-    if (pl.max_tasks < 1) return PKV_ERR_INVALID;
+  } else if (defer && pl.stages <= 4) {
+    pl.max_tasks = 4 * pl.warps;   // balanced mode: slots 2 t, 2 t + 1 of task t
     pl.n_slots = 2 * static_cast<int64_t>(pl.max_tasks);
   } else {
     pl.n_slots = 2 * static_cast<int64_t>(pl.warps);
@@ -443,6 +450,13 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   pl.off_ml = round_up(count_bytes, 256);
   pl.off_o = pl.off_ml + round_up(static_cast<size_t>(pl.n_slots) * g * 2 * sizeof(float), 256);
   pl.ws_bytes = pl.off_o + static_cast<size_t>(pl.n_slots) * g * d.head_dim * sizeof(float);
+  // deferred mode (at most 4 stages: each warp's stage tasks live in the CTA's scan scratch): after
+  // the partials, [part_chunks, T1, T2, NP1 (2 words), pref[0..n], ipref[0..n]] for the merge kernel
+  pl.defer = defer && pl.stages <= 4;
+  if (pl.defer) {
+    pl.off_meta = round_up(pl.ws_bytes, 256);
+    pl.ws_bytes = pl.off_meta + (5 + 2 * (static_cast<size_t>(n_seqs) + 1)) * sizeof(int32_t);
+  }
   *out = pl;
   return PKV_OK;
 }
@@ -452,7 +466,11 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
                          const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads, float scale,
                          int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
                          void* stream, int32_t start = 0, float* lse_out = nullptr,
-                         int32_t* defer_meta = nullptr, int32_t late_wait = 0, unsigned long long tag = 0);
+                         bool defer = false, int32_t late_wait = 0, unsigned long long tag = 0,
+                         DecodePlan* plan_out = nullptr);
+pkv_status merge_launch(const pkv_pool* p, const DecodePlan& pl, unsigned char* ws, float* out, int32_t n_seqs,
+                        int32_t Hq, const float* lse_s, const float* part_o, const float* part_lse, int32_t n_split,
+                        const int32_t* block_tables, int32_t prefix_blocks, cudaStream_t s);
 
 }  // namespace
 
@@ -587,7 +605,8 @@ pkv_status pkv_paged_prefill(const pkv_pool* p, float* out, const void* q, const
 size_t pkv_decode_workspace_bytes(const pkv_pool* p, int32_t n_seqs, int32_t num_q_heads, int32_t partition_tokens) {
   if (!p) return 0;
   DecodePlan pl;
-  if (plan_decode(p, n_seqs, num_q_heads, partition_tokens, 0, &pl) != PKV_OK) return 0;
+  if (plan_decode(p, n_seqs, num_q_heads, partition_tokens, 0, &pl, decode_defer_wanted(partition_tokens)) != PKV_OK)
+    return 0;
   return pl.ws_bytes;
 }
 
@@ -604,8 +623,14 @@ pkv_status pkv_paged_decode_window(const pkv_pool* p, float* out, const void* q,
                                    int32_t n_seqs, int32_t num_q_heads, float scale, int32_t window,
                                    int32_t partition_tokens, void* workspace, size_t workspace_bytes, void* stream) {
   if (p && p->desc.dtype == PKV_FP8) return PKV_ERR_INVALID;   // pkv_paged_decode_fp8
-  return decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs,
-                       num_q_heads, scale, window, partition_tokens, workspace, workspace_bytes, stream);
+  DecodePlan pl;
+  const pkv_status r =
+      decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs, num_q_heads,
+                    scale, window, partition_tokens, workspace, workspace_bytes, stream, 0, nullptr,
+                    decode_defer_wanted(partition_tokens), 0, 0, &pl);
+  if (r != PKV_OK || n_seqs == 0 || !pl.defer) return r;
+  return merge_launch(p, pl, static_cast<unsigned char*>(workspace), out, n_seqs, num_q_heads, nullptr, nullptr,
+                      nullptr, 0, block_tables, 0, static_cast<cudaStream_t>(stream));
 }
 
 pkv_status pkv_paged_decode_fp8(const pkv_pool* p, float* out, const void* q, const void* k_cache,
@@ -615,8 +640,14 @@ pkv_status pkv_paged_decode_fp8(const pkv_pool* p, float* out, const void* q, co
                                 void* workspace, size_t workspace_bytes, void* stream) {
   if (!p || p->desc.dtype != PKV_FP8) return PKV_ERR_INVALID;
   if (n_seqs > 0 && (!k_scale || !v_scale || !aligned16(k_scale) || !aligned16(v_scale))) return PKV_ERR_INVALID;
-  return decode_launch(p, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, n_seqs,
-                       num_q_heads, scale, window, partition_tokens, workspace, workspace_bytes, stream);
+  DecodePlan pl;
+  const pkv_status r =
+      decode_launch(p, out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, n_seqs, num_q_heads,
+                    scale, window, partition_tokens, workspace, workspace_bytes, stream, 0, nullptr,
+                    decode_defer_wanted(partition_tokens), 0, 0, &pl);
+  if (r != PKV_OK || n_seqs == 0 || !pl.defer) return r;
+  return merge_launch(p, pl, static_cast<unsigned char*>(workspace), out, n_seqs, num_q_heads, nullptr, nullptr,
+                      nullptr, 0, block_tables, 0, static_cast<cudaStream_t>(stream));
 }
 
 pkv_status pkv_reshape_and_cache_fp8(const pkv_pool* p, const void* k, const void* v, const int64_t* slots,
@@ -687,8 +718,8 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
                          const float* k_scale, const float* v_scale, const int32_t* block_tables,
                          const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads, float scale,
                          int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
-                         void* stream, int32_t start, float* lse_out, int32_t* defer_meta,
-                         int32_t late_wait, unsigned long long tag) {
+                         void* stream, int32_t start, float* lse_out, bool defer_req,
+                         int32_t late_wait, unsigned long long tag, DecodePlan* plan_out) {
   if (!p || window < 0) return PKV_ERR_INVALID;
   if (n_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID;
@@ -697,9 +728,9 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
     return PKV_ERR_INVALID;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PKV_ERR_INVALID;
   DecodePlan pl;
-  const bool defer = defer_meta != nullptr && partition_tokens == 0;
   const pkv_status st =
-      plan_decode(p, n_seqs, num_q_heads, partition_tokens, (window > 0 || start > 0) ? 1 : 0, &pl, defer);
+      plan_decode(p, n_seqs, num_q_heads, partition_tokens, (window > 0 || start > 0) ? 1 : 0, &pl, defer_req);
+  const bool defer = pl.defer;
   if (st != PKV_OK) return st;
   if (workspace_bytes < pl.ws_bytes || (pl.ws_bytes > 0 && (!workspace || !aligned16(workspace))))
     return PKV_ERR_INVALID;
@@ -750,7 +781,7 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   a.err = p->d_err_word;
   a.start = start;
   a.lse_out = lse_out;
-  a.defer_meta = defer ? defer_meta : nullptr;
+  a.defer_meta = defer ? reinterpret_cast<int32_t*>(ws + pl.off_meta) : nullptr;
   a.max_tasks = pl.max_tasks;
   // deferred mode: chunks per task (no arrivals, so cutting units costs no fences; small tasks balance)
   if (defer) a.min_chunks = env_int("PKV_CASCADE_TASK_CHUNKS", 16);
@@ -758,6 +789,45 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   a.late_wait = late_wait;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (plan_out) *plan_out = pl;
+  return PKV_OK;
+}
+
+// The merge kernel after a deferred-mode decode (plan pl, workspace ws): the rows of units cut by
+// task boundaries, and with n_split > 0 the shared-prefix splits of every row.
+pkv_status merge_launch(const pkv_pool* p, const DecodePlan& pl, unsigned char* ws, float* out, int32_t n_seqs,
+                        int32_t Hq, const float* lse_s, const float* part_o, const float* part_lse, int32_t n_split,
+                        const int32_t* block_tables, int32_t prefix_blocks, cudaStream_t s) {
+  const pkv_pool_desc& d = p->desc;
+  pkv_dev::CascadeMergeArgs m;
+  m.out = out;
+  m.lse_s = lse_s;
+  m.part_o = part_o;
+  m.part_lse = part_lse;
+  m.dec_o = reinterpret_cast<const float*>(ws + pl.off_o);
+  m.dec_ml = reinterpret_cast<const float*>(ws + pl.off_ml);
+  m.meta = reinterpret_cast<const int32_t*>(ws + pl.off_meta);
+  m.max_parts = pl.max_parts;
+  m.task_ctr = reinterpret_cast<unsigned long long*>(ws);   // the decode's first workspace word
+  m.tables = block_tables;
+  m.n_rows = static_cast<int64_t>(n_seqs) * Hq;
+  m.D = d.head_dim;
+  m.G = Hq / d.num_kv_heads;
+  m.Hkv = d.num_kv_heads;
+  m.n_split = n_split;
+  m.MB = d.max_blocks_per_seq;
+  m.n_seqs = n_seqs;
+  m.prefix_blocks = prefix_blocks;
+  m.err = p->d_err_word;
+  // one wave: a warp per row, rows beyond the resident warps taken grid-stride
+  const int per_sm = occupancy(reinterpret_cast<const void*>(pkv_dev::merge_prefix_kernel), 256, 0);
+  const int64_t wave = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * num_sms();
+  const int64_t want = (m.n_rows + 7) / 8;
+  const int64_t blocks = want < wave ? want : wave;
+  if (launch(pkv_dev::merge_prefix_kernel, dim3(static_cast<unsigned>(blocks > 0 ? blocks : 1)), dim3(256), 0, s,
+             m) != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
@@ -772,7 +842,7 @@ struct SharedPlan {
   DecodePlan dec;
   int32_t shared_len = 0, split_keys = 0, n_split = 0, item_tokens = 0;
   int64_t grid_items = 0;
-  size_t off_meta = 0, off_lse = 0, off_plse = 0, off_po = 0, bytes = 0;
+  size_t off_lse = 0, off_plse = 0, off_po = 0, bytes = 0;
 };
 
 pkv_status plan_shared(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t prefix_blocks, SharedPlan* out) {
@@ -805,8 +875,8 @@ pkv_status plan_shared(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pr
   sp.n_split = (sp.shared_len + sp.split_keys - 1) / sp.split_keys;
   sp.grid_items = items_per_split * sp.n_split;
   const size_t rows = static_cast<size_t>(n_seqs) * Hq;
-  sp.off_meta = round_up(sp.dec.ws_bytes, 256);
-  sp.off_lse = sp.off_meta + round_up((static_cast<size_t>(n_seqs) + 5) * sizeof(int32_t), 256);
+  if (!sp.dec.defer) return PKV_ERR_INVALID;
+  sp.off_lse = round_up(sp.dec.ws_bytes, 256);
   sp.off_plse = sp.off_lse + round_up(rows * sizeof(float), 256);
   sp.off_po = sp.off_plse + round_up(static_cast<size_t>(sp.n_split) * rows * sizeof(float), 256);
   sp.bytes = sp.off_po + static_cast<size_t>(sp.n_split) * rows * d.head_dim * sizeof(float);
@@ -851,7 +921,6 @@ pkv_status pkv_paged_decode_shared_prefix(const pkv_pool* p, float* out, const v
   float* lse_s = reinterpret_cast<float*>(ws + sp.off_lse);
   float* part_lse = reinterpret_cast<float*>(ws + sp.off_plse);
   float* part_o = reinterpret_cast<float*>(ws + sp.off_po);
-  int32_t* meta = reinterpret_cast<int32_t*>(ws + sp.off_meta);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // 1. the shared prefix once for every row: tensor-core kernel in shared-prefix mode, key splits.
   // Once past its own dependency wait it lets the decode launch: decode CTAs take the SMs it leaves
@@ -889,38 +958,11 @@ pkv_status pkv_paged_decode_shared_prefix(const pkv_pool* p, float* out, const v
   // reads nothing step 1 writes; it waits for step 1 only before it completes, so that step 3 (which
   // waits for it) sees both.
   r = decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs, num_q_heads,
-                    scale, 0, 0, workspace, sp.dec.ws_bytes, stream, sp.shared_len, lse_s, meta, 1, tag);
+                    scale, 0, 0, workspace, sp.dec.ws_bytes, stream, sp.shared_len, lse_s, true, 1, tag);
   if (r != PKV_OK) return r;
-  // 3. log-sum-exp merge of every row's parts: suffix (final row or split-unit partials) and prefix splits
-  pkv_dev::CascadeMergeArgs m;
-  m.out = out;
-  m.lse_s = lse_s;
-  m.part_o = part_o;
-  m.part_lse = part_lse;
-  m.dec_o = reinterpret_cast<const float*>(ws + sp.dec.off_o);
-  m.dec_ml = reinterpret_cast<const float*>(ws + sp.dec.off_ml);
-  m.meta = meta;
-  m.task_ctr = reinterpret_cast<unsigned long long*>(ws);   // the decode's first workspace word
-  m.tables = block_tables;
-  m.n_rows = static_cast<int64_t>(n_seqs) * num_q_heads;
-  m.D = d.head_dim;
-  m.G = num_q_heads / d.num_kv_heads;
-  m.Hkv = d.num_kv_heads;
-  m.n_split = sp.n_split;
-  m.MB = d.max_blocks_per_seq;
-  m.n_seqs = n_seqs;
-  m.prefix_blocks = prefix_blocks;
-  m.err = p->d_err_word;
-  // one wave: a warp per row, rows beyond the resident warps taken grid-stride
-  const int per_sm = occupancy(reinterpret_cast<const void*>(pkv_dev::merge_prefix_kernel), 256, 0);
-  const int64_t wave = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * num_sms();
-  const int64_t want = (m.n_rows + 7) / 8;
-  const int64_t blocks = want < wave ? want : wave;
-  if (launch(pkv_dev::merge_prefix_kernel, dim3(static_cast<unsigned>(blocks > 0 ? blocks : 1)), dim3(256), 0, s,
-             m) != cudaSuccess ||
-      cudaGetLastError() != cudaSuccess)
-    return PKV_ERR_CUDA;
-  return PKV_OK;
+  // 3. log-sum-exp merge of every row's parts: suffix (final row or cut-unit partials) and prefix splits
+  return merge_launch(p, sp.dec, ws, out, n_seqs, num_q_heads, lse_s, part_o, part_lse, sp.n_split, block_tables,
+                      prefix_blocks, s);
 }
 
 }  // extern "C"
