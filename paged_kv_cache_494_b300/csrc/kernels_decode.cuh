@@ -78,7 +78,6 @@ struct DecodeArgs {
                                  // partial in its slot, and block 0 writes [T, pref[0..n]] here for the
                                  // later kernel that merges them
   int32_t max_tasks;             // deferred mode: slots for at most this many tasks (2 per task)
-  int32_t early_trigger;         // non-zero: the next kernel may launch once this one passed its own wait
   int32_t late_wait;             // non-zero: this kernel reads nothing the previous kernel writes (that one let
                                  // it launch once its own inputs were complete); it waits for the previous
                                  // kernel only before it completes
@@ -1257,7 +1256,6 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   if (threadIdx.x < NW) cta_cnt[threadIdx.x] = 0;
   set_error_word(a.err);
   if (!a.late_wait) pdl_wait();
-  if (a.early_trigger) pdl_launch_dependents();
   // deferred mode: the CTA's first tasks, one per warp, taken at once, while the prefix is built
   // (wsum[8] is not used by the prefix build)
   if (a.defer_meta != nullptr && threadIdx.x == 0)

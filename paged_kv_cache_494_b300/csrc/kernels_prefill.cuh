@@ -39,8 +39,6 @@ struct PrefillArgs {
   float* part_o;
   float* part_lse;
   int32_t early_trigger;   // tcgen05 kernel: the next kernel may launch once this one passed its own wait
-  int32_t late_wait;       // tcgen05 kernel: reads nothing the previous kernel writes (that one let it
-                           // launch once its own inputs were complete); waits for it only before completing
   unsigned long long* task_ctr;   // optional: the following decode's task counter, set to its call tag
   unsigned long long task_tag;    //   here so that its first takers find it installed
 };

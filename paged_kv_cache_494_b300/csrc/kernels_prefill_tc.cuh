@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
   int32_t* tpref = wsum + 64;
 
   set_error_word(a.err);
-  if (!a.late_wait) pdl_wait();   // before any global access, and before holding tensor memory
+  pdl_wait();   // before any global access, and before holding tensor memory
   if (a.early_trigger) pdl_launch_dependents();
   if (a.task_ctr != nullptr && blockIdx.x == 0 && tid == 0) install_task_tag(a.task_ctr, a.task_tag);
 
@@ -300,7 +300,6 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
   const int32_t n_split = shared ? (a.shared_len + a.split_keys - 1) / a.split_keys : 1;
   const int64_t n_slots = shared ? static_cast<int64_t>(n_split) * per_level : static_cast<int64_t>(*max_items) * per_level;
   if (static_cast<int64_t>(blockIdx.x) >= n_slots) {
-    if (a.late_wait) pdl_wait();
     pdl_launch_dependents();
     return;
   }
@@ -768,7 +767,6 @@ __global__ void __launch_bounds__(TcShape<D, G, NT, STAGES>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, Sh::TMEM_COLS);
   }
-  if (a.late_wait) pdl_wait();
   pdl_launch_dependents();
 }
 

@@ -62,7 +62,7 @@ int num_sms() {
 // Programmatic dependent launch on every libpagedkv kernel unless PKV_PDL=0. Each kernel waits for
 // its predecessor in the stream (griddepcontrol.wait) before touching global memory, so only the
 // launch latency overlaps and data ordering is plain stream order; the one exception is the
-// shared-prefix decode, whose middle kernel reads nothing its predecessor writes and waits for it
+// shared-prefix decode, whose decode kernel reads nothing its predecessor writes and waits for it
 // only before completing (the tensor-core kernel lets it launch once its own inputs are complete).
 bool pdl_enabled() {
   static const bool on = [] {
@@ -467,7 +467,7 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
                          int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
                          void* stream, int32_t start = 0, float* lse_out = nullptr,
                          bool defer = false, int32_t late_wait = 0, unsigned long long tag = 0,
-                         DecodePlan* plan_out = nullptr, int32_t early_trigger = 0);
+                         DecodePlan* plan_out = nullptr);
 pkv_status merge_launch(const pkv_pool* p, const DecodePlan& pl, unsigned char* ws, float* out, int32_t n_seqs,
                         int32_t Hq, const float* lse_s, const float* part_o, const float* part_lse, int32_t n_split,
                         const int32_t* block_tables, int32_t prefix_blocks, cudaStream_t s);
@@ -719,7 +719,7 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
                          const int32_t* context_lens, int32_t n_seqs, int32_t num_q_heads, float scale,
                          int32_t window, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
                          void* stream, int32_t start, float* lse_out, bool defer_req,
-                         int32_t late_wait, unsigned long long tag, DecodePlan* plan_out, int32_t early_trigger) {
+                         int32_t late_wait, unsigned long long tag, DecodePlan* plan_out) {
   if (!p || window < 0) return PKV_ERR_INVALID;
   if (n_seqs == 0) return PKV_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID;
@@ -785,7 +785,6 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   a.max_tasks = pl.max_tasks;
   // deferred mode: chunks per task (no arrivals, so cutting units costs no fences; small tasks balance)
   if (defer) a.min_chunks = env_int("PKV_CASCADE_TASK_CHUNKS", 16);
-  a.early_trigger = early_trigger;
   a.late_wait = late_wait;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||
@@ -866,9 +865,7 @@ pkv_status plan_shared(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pr
   const int64_t items_per_split = (static_cast<int64_t>(n_seqs) + sp.item_tokens - 1) / sp.item_tokens * d.num_kv_heads;
   const int sms = num_sms();
   if (sms <= 0) return PKV_ERR_CUDA;
-  // (decode first, PKV_CASCADE_ORDER=1: the prefix kernel runs on SMs the decode has left, one item each)
-  const int target = env_int("PKV_CASCADE_ORDER", 0) == 1 ? sms : sms / 4;
-  int64_t ns = (target + items_per_split / 2) / items_per_split;
+  int64_t ns = (sms / 4 + items_per_split / 2) / items_per_split;
   const int64_t max_split = (sp.shared_len + 63) / 64;
   ns = ns < 1 ? 1 : (ns > max_split ? max_split : ns);
   sp.split_keys = static_cast<int32_t>(((sp.shared_len + ns - 1) / ns + 63) / 64 * 64);
@@ -924,11 +921,9 @@ pkv_status pkv_paged_decode_shared_prefix(const pkv_pool* p, float* out, const v
   float* part_lse = reinterpret_cast<float*>(ws + sp.off_plse);
   float* part_o = reinterpret_cast<float*>(ws + sp.off_po);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Two orders (PKV_CASCADE_ORDER: 0 prefix kernel first, 1 decode first); in both the second kernel
-  // reads nothing the first writes, launches once the first is past its own dependency wait, and
-  // waits for the first only before completing, so that the merge (which waits for the second) sees
-  // both.
-  const bool decode_first = env_int("PKV_CASCADE_ORDER", 0) == 1;
+  // 1. the shared prefix once for every row (tensor-core kernel, key splits); once past its own
+  // dependency wait it lets the decode launch (decode CTAs take the SMs it leaves free and, by dynamic
+  // tasks, the rest as its CTAs finish), and it installs the decode's call tag in the task counter.
   pkv_dev::PrefillArgs a;
   std::memset(&a, 0, sizeof a);
   a.out = nullptr;
@@ -951,33 +946,19 @@ pkv_status pkv_paged_decode_shared_prefix(const pkv_pool* p, float* out, const v
   a.split_keys = sp.split_keys;
   a.part_o = part_o;
   a.part_lse = part_lse;
+  a.early_trigger = 1;
   const unsigned long long tag = next_call_tag();   // the decode's call tag
-  pkv_status r;
-  if (!decode_first) {
-    // 1. the shared prefix once for every row (tensor-core kernel, key splits); it lets the decode
-    // launch at once (decode CTAs take the SMs it leaves free and, by dynamic tasks, the rest as its
-    // CTAs finish) and installs the decode's tag in the task counter.
-    a.early_trigger = 1;
-    a.task_ctr = reinterpret_cast<unsigned long long*>(ws);
-    a.task_tag = tag;
-    r = tc_prefill_launch(p, a, k_cache, v_cache, s, sp.grid_items);
-    if (r != PKV_OK) return r;
-    // 2. private suffixes: decode over positions [shared_len, len) with each row's log-sum-exp, in
-    // deferred-merge mode (dynamic tasks; units cut by task boundaries leave partials for step 3).
-    r = decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs,
-                      num_q_heads, scale, 0, 0, workspace, sp.dec.ws_bytes, stream, sp.shared_len, lse_s, true, 1,
-                      tag);
-    if (r != PKV_OK) return r;
-  } else {
-    // 1. private suffixes first, on every SM; 2. the prefix kernel takes SMs as decode CTAs leave.
-    r = decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs,
-                      num_q_heads, scale, 0, 0, workspace, sp.dec.ws_bytes, stream, sp.shared_len, lse_s, true, 0,
-                      tag, nullptr, 1);
-    if (r != PKV_OK) return r;
-    a.late_wait = 1;
-    r = tc_prefill_launch(p, a, k_cache, v_cache, s, sp.grid_items);
-    if (r != PKV_OK) return r;
-  }
+  a.task_ctr = reinterpret_cast<unsigned long long*>(ws);
+  a.task_tag = tag;
+  pkv_status r = tc_prefill_launch(p, a, k_cache, v_cache, s, sp.grid_items);
+  if (r != PKV_OK) return r;
+  // 2. private suffixes: decode over positions [shared_len, len) with each row's log-sum-exp, in
+  // deferred-merge mode (dynamic tasks; units cut by task boundaries leave partials for step 3). It
+  // reads nothing step 1 writes and waits for step 1 only before completing, so that step 3 (which
+  // waits for it) sees both.
+  r = decode_launch(p, out, q, k_cache, v_cache, nullptr, nullptr, block_tables, context_lens, n_seqs, num_q_heads,
+                    scale, 0, 0, workspace, sp.dec.ws_bytes, stream, sp.shared_len, lse_s, true, 1, tag);
+  if (r != PKV_OK) return r;
   // 3. log-sum-exp merge of every row's parts: suffix (final row or cut-unit partials) and prefix splits
   return merge_launch(p, sp.dec, ws, out, n_seqs, num_q_heads, lse_s, part_o, part_lse, sp.n_split, block_tables,
                       prefix_blocks, s);
