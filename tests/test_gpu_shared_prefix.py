@@ -180,3 +180,39 @@ def test_repeat_calls_and_cuda_graph_replays_are_bitwise_equal():
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
     assert pkv.last_error() == pkv.OK
+
+
+def test_one_workspace_across_shapes_bitwise(monkeypatch):
+    """One workspace serves shared-prefix calls of different batch sizes and prefix lengths in turn,
+    with deferred plain decodes in between (another user of the same task counter): every call returns
+    exactly what it returns on a fresh NaN-filled workspace, so stale counters, tags and partials left
+    by earlier calls are never taken for its own."""
+    monkeypatch.setenv("PKV_DECODE_DEFER", "1")
+    c = forked(512, list(range(0, 400, 7)), Hq=16, Hkv=4, D=128, B=16, seed=9)
+    pb_full = c.pool.shared_prefix_blocks(c.seqs)
+    shapes = [(c.n, pb_full), (c.n // 2, pb_full), (c.n, 7), (c.n // 3, 20)]
+    nbytes = max(max(c.pool.shared_prefix_workspace_bytes(n, c.Hq, pb) for n, pb in shapes),
+                 c.pool.decode_workspace_bytes(c.n, c.Hq, 0))
+
+    def run(n, pb, ws):
+        out = torch.full((n, c.Hq, c.D), float("nan"), dtype=torch.float32, device="cuda")
+        c.pool.paged_decode_shared_prefix(out, c.q[:n], c.k_cache, c.v_cache, c.tables[:n], c.lens[:n], c.scale,
+                                          pb, workspace=ws)
+        torch.cuda.synchronize()
+        return out
+
+    def nan_ws():
+        return torch.full((nbytes // 4 + 4,), float("nan"), dtype=torch.float32, device="cuda")
+
+    fresh = {s: run(*s, nan_ws()) for s in shapes}
+    ref = c.oracle_decode()
+    for (n, pb), out in fresh.items():
+        assert max_err(out, ref[:n]) <= TOL["bf16"]
+    ws = nan_ws()
+    plain = torch.empty(c.n, c.Hq, c.D, device="cuda")
+    for it in range(12):
+        s = shapes[it % len(shapes)]
+        assert torch.equal(run(*s, ws), fresh[s]), (it, s)
+        if it % 3 == 2:   # a deferred plain decode on the same workspace
+            c.pool.paged_decode(plain, c.q, c.k_cache, c.v_cache, c.tables, c.lens, c.scale, workspace=ws)
+    assert pkv.last_error() == pkv.OK
