@@ -374,11 +374,14 @@ struct DecodePlan {
 };
 
 // Deferred-merge decode (dynamic tasks, then the merge kernel) for pkv_paged_decode(_window, _fp8)
-// when PKV_DECODE_DEFER=1; otherwise the in-kernel merge. Measured on B300 the deferred form is the
-// slower one for a whole batch (every task pays its own setup: locate, length and query loads, which a
-// static range pays once per unit): serving batch 0.826 against 0.868 of the copy bandwidth, 8 x 32k
-// tokens 217 / 248 us (512-token partitions / balanced) against 209 / 210 us. The shared-prefix decode
-// always uses it, since its merge kernel runs anyway and its decode starts beside another kernel.
+// when PKV_DECODE_DEFER=1; otherwise the in-kernel merge. Measured on B300 (same box, L2 flushed):
+// balanced split, deferred is slower (every task pays its own setup: locate, length and query loads,
+// which a static range pays once per unit): serving batch 0.826 against 0.868 of the copy bandwidth,
+// 8 x 32k tokens 248 against 210 us; 512-token partitions, it wins on long contexts (8 x 32k: 217 against
+// 223-228 us) and loses on medium ones (64 sequences, G 5: 72 against 64 us; 128 children of a shared
+// prompt: 101 against 90 us); the host does not know the lengths, so the default stays in-kernel. The
+// shared-prefix decode always uses it: its merge kernel runs anyway and its decode starts beside another
+// kernel.
 bool decode_defer_wanted(int32_t) { return env_int("PKV_DECODE_DEFER", 0) > 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
