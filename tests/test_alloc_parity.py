@@ -142,6 +142,10 @@ def test_shared_prefix_blocks_hand_worked():
     assert lib.shared_prefix_blocks([c0, other]) == 0
     with pytest.raises(pkv.PagedKVError):
         lib.shared_prefix_blocks([])
+    lib.free(other)
+    with pytest.raises(pkv.PagedKVError) as e:              # a freed sequence id
+        lib.shared_prefix_blocks([c0, other])
+    assert e.value.status == pkv.ERR_NO_SEQ
 
 
 def test_large_pool_constructs_fast():
