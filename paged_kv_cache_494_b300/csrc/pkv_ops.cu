@@ -104,6 +104,7 @@ enum MapKind { MAPS_NONE = 0, MAPS_BF16 = 1, MAPS_FP8 = 2 };
 
 struct KernelPair {
   DecodeKernel decode = nullptr;
+  DecodeKernel decode_defer = nullptr;   // the deferred-merge instantiation (bf16 pools only)
   int stage_bytes = 0;
   int maps = MAPS_NONE;   // which tensor maps the staging needs (1-D bulk copies when none)
 };
@@ -111,7 +112,7 @@ struct KernelPair {
 template <class Math, int D, int G>
 KernelPair pair_for(int maps) {
   KernelPair k;
-  k.decode = pkv_dev::paged_decode_kernel<Math, D, G>;
+  k.decode = pkv_dev::paged_decode_kernel<Math, D, G, false>;
   k.stage_bytes = Math::kStageBytes;
   k.maps = maps;
   return k;
@@ -119,8 +120,14 @@ KernelPair pair_for(int maps) {
 
 template <int D, int G>
 KernelPair pick_bf16(bool simt) {
-  if (simt) return pair_for<pkv_dev::SimtMath<__nv_bfloat16, D, G>, D, G>(MAPS_NONE);
-  return pair_for<pkv_dev::MmaMath<D, G>, D, G>(MAPS_BF16);
+  if (simt) {
+    KernelPair k = pair_for<pkv_dev::SimtMath<__nv_bfloat16, D, G>, D, G>(MAPS_NONE);
+    k.decode_defer = pkv_dev::paged_decode_kernel<pkv_dev::SimtMath<__nv_bfloat16, D, G>, D, G, true>;
+    return k;
+  }
+  KernelPair k = pair_for<pkv_dev::MmaMath<D, G>, D, G>(MAPS_BF16);
+  k.decode_defer = pkv_dev::paged_decode_kernel<pkv_dev::MmaMath<D, G>, D, G, true>;
+  return k;
 }
 
 template <int D>
@@ -425,13 +432,17 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   pl.nw = env_int("PKV_DECODE_WARPS", 4);
   if (pl.nw > 4) pl.nw = 4;   // the decode kernels are compiled for at most 128 threads per CTA
   pl.stages = env_int("PKV_DECODE_STAGES", 2);
+  // deferred mode: bf16 pools (the only ones with a deferred instantiation), at most 4 stages (each
+  // warp's stage tasks live in the CTA's scan scratch)
+  pl.defer = defer && pl.k.decode_defer != nullptr && pl.stages <= 4;
+  const void* kern = reinterpret_cast<const void*>(pl.defer ? pl.k.decode_defer : pl.k.decode);
   pl.smem = pkv_dev::decode_smem_bytes(pl.nw, pl.stages, pl.k.stage_bytes, n_seqs, partition_tokens > 0, window > 0);
   // every CTA keeps per-sequence prefix sums in shared memory: the batch must fit beside the ring
   const size_t smem_max = max_smem_optin();
   if (smem_max == 0) return PKV_ERR_CUDA;
   if (pl.smem > smem_max) return PKV_ERR_INVALID;
-  if (!ensure_smem(reinterpret_cast<const void*>(pl.k.decode), pl.smem)) return PKV_ERR_CUDA;
-  const int per_sm = occupancy(reinterpret_cast<const void*>(pl.k.decode), pl.nw * 32, pl.smem);
+  if (!ensure_smem(kern, pl.smem)) return PKV_ERR_CUDA;
+  const int per_sm = occupancy(kern, pl.nw * 32, pl.smem);
   const int sms = num_sms();
   if (per_sm <= 0 || sms <= 0) return PKV_ERR_CUDA;
   pl.grid = sms * per_sm;
@@ -442,7 +453,7 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
     const int64_t max_chunks = (static_cast<int64_t>(d.max_blocks_per_seq) * d.block_size) / pkv_dev::kChunk;
     pl.max_parts = static_cast<int>((max_chunks + pl.part_chunks - 1) / pl.part_chunks);
     pl.n_slots = pl.n_units * pl.max_parts;
-  } else if (defer && pl.stages <= 4) {
+  } else if (pl.defer) {
     pl.max_tasks = 4 * pl.warps;   // balanced mode: slots 2 t, 2 t + 1 of task t
     pl.n_slots = 2 * static_cast<int64_t>(pl.max_tasks);
   } else {
@@ -453,9 +464,8 @@ pkv_status plan_decode(const pkv_pool* p, int32_t n_seqs, int32_t Hq, int32_t pa
   pl.off_ml = round_up(count_bytes, 256);
   pl.off_o = pl.off_ml + round_up(static_cast<size_t>(pl.n_slots) * g * 2 * sizeof(float), 256);
   pl.ws_bytes = pl.off_o + static_cast<size_t>(pl.n_slots) * g * d.head_dim * sizeof(float);
-  // deferred mode (at most 4 stages: each warp's stage tasks live in the CTA's scan scratch): after
-  // the partials, [part_chunks, T1, T2, NP1 (2 words), pref[0..n], ipref[0..n]] for the merge kernel
-  pl.defer = defer && pl.stages <= 4;
+  // deferred mode: after the partials, [part_chunks, T1, T2, NP1 (2 words), pref[0..n], ipref[0..n]]
+  // for the merge kernel
   if (pl.defer) {
     pl.off_meta = round_up(pl.ws_bytes, 256);
     pl.ws_bytes = pl.off_meta + (5 + 2 * (static_cast<size_t>(n_seqs) + 1)) * sizeof(int32_t);
@@ -790,7 +800,8 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
   if (defer) a.min_chunks = env_int("PKV_CASCADE_TASK_CHUNKS", 16);
   a.late_wait = late_wait;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch(pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) != cudaSuccess ||
+  if (launch(pl.defer ? pl.k.decode_defer : pl.k.decode, dim3(pl.grid), dim3(pl.nw * 32), pl.smem, s, a, maps) !=
+          cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
     return PKV_ERR_CUDA;
   if (plan_out) *plan_out = pl;

@@ -319,9 +319,10 @@ def test_cuda_graph_replays_match_direct_calls_bitwise(pt, path):
 @pytest.mark.parametrize("name,pt,window", [("gqa5_bf16", 0, 0), ("gqa5_bf16", 512, 0), ("tiny_f32", 64, 0),
                                             ("prefix_cow_partial_bf16", 0, 300), ("gqa5_bf16", 32, 100)])
 def test_deferred_merge_mode(name, pt, window, monkeypatch):
-    """PKV_DECODE_DEFER=1: dynamic tasks in the decode, cut units merged by a second kernel. Same
-    results as the oracle for both split modes, a window, fp32 and bf16; repeated calls agree bit for
-    bit (a task's chunks, and so its result, do not depend on which warp takes it)."""
+    """PKV_DECODE_DEFER=1: dynamic tasks in the decode, cut units merged by a second kernel (bf16
+    pools; an fp32 pool has no deferred instantiation and keeps the in-kernel merge). Same results as
+    the oracle for both split modes and a window; repeated calls agree bit for bit (a task's chunks,
+    and so its result, do not depend on which warp takes it)."""
     monkeypatch.setenv("PKV_DECODE_DEFER", "1")
     c = case_from_workload(name)
     out = c.gpu_decode(pt, window=window)
