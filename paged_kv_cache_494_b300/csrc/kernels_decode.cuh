@@ -816,7 +816,10 @@ struct Fp8Math {
     const int32_t off = static_cast<int32_t>(row0 - page * a.B);
     mbar_arrive_expect_tx(bar, kTxBytes);
     tma_load_2d(dst, &maps.k, 0, static_cast<int32_t>(row0), bar, policy);
-    tma_load_2d(dst + KBOX, &maps.v, off, static_cast<int32_t>(page * D), bar, policy);
+    if (a.B == kChunk)   // the chunk is the whole V page of this (block, head): one contiguous 2 KB run
+      bulk_g2s_hint(dst + KBOX, static_cast<const unsigned char*>(a.v_cache) + page * VBOX, VBOX, bar, policy);
+    else                 // a 16-token column slice of a wider page: 2-D box
+      tma_load_2d(dst + KBOX, &maps.v, off, static_cast<int32_t>(page * D), bar, policy);
     bulk_g2s_hint(dst + kScaleOff, a.k_scale + row0, kChunk * 4, bar, policy);
     bulk_g2s_hint(dst + kScaleOff + kChunk * 4, a.v_scale + row0, kChunk * 4, bar, policy);
   }
