@@ -594,10 +594,17 @@ struct MmaMath {
                                uint64_t policy) {
     mbar_arrive_expect_tx(bar, 2 * CB);
     const int32_t y = static_cast<int32_t>(row0);
+    if constexpr (KB == 2) {
+      // 3-D maps (64 dims, rows, the row's two halves): one copy per operand lands as the two
+      // 16-row x 128-byte boxes, half after half, with the same swizzle
+      tma_load_3d_hint(dst, &maps.k, 0, y, 0, bar, policy);
+      tma_load_3d_hint(dst + CB, &maps.v, 0, y, 0, bar, policy);
+    } else {
 #pragma unroll
-    for (int kb = 0; kb < KB; ++kb) {
-      tma_load_2d(dst + kb * BOX, &maps.k, 64 * kb, y, bar, policy);
-      tma_load_2d(dst + CB + kb * BOX, &maps.v, 64 * kb, y, bar, policy);
+      for (int kb = 0; kb < KB; ++kb) {
+        tma_load_2d(dst + kb * BOX, &maps.k, 64 * kb, y, bar, policy);
+        tma_load_2d(dst + CB + kb * BOX, &maps.v, 64 * kb, y, bar, policy);
+      }
     }
   }
 

@@ -245,6 +245,22 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const pkv_pool_desc& d) 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 pools with head_dim 128, for the decode: the [rows][128] array viewed as 3-D (64 dims, rows,
+// the two 128-byte halves of a row; the halves' stride, 128 bytes, is the outer one), boxes of
+// 64 x 16 x 2 with 128-byte swizzle: one copy brings a chunk's K (or V) as the two boxes of the 2-D
+// map, half after half.
+bool encode_cache_map_halves(CUtensorMap* m, const void* base, const pkv_pool_desc& d) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn || d.head_dim != 128) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(d.num_blocks) * d.num_kv_heads * d.block_size, 2};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d.head_dim) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pkv_dev::kChunk), 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // fp8 pools: K codes as a 2-D uint8 [NB*Hkv*B rows][D] array (boxes of 16 rows x 128 bytes, 128-byte
 // swizzle); V codes as a 2-D uint8 [NB*Hkv*D rows][B] array (dim-major pages; boxes of 128 rows x
 // 16 bytes, no swizzle).
@@ -777,7 +793,10 @@ pkv_status decode_launch(const pkv_pool* p, float* out, const void* q, const voi
     const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.num_kv_heads * d.block_size *
                          (pl.k.maps == MAPS_FP8 ? d.head_dim / d.block_size + 1 : 1);
     if (rows > 0x7fffffffLL) return PKV_ERR_INVALID;   // tensor coordinates are 32-bit
-    if (pl.k.maps == MAPS_BF16) {
+    if (pl.k.maps == MAPS_BF16 && d.head_dim == 128) {   // MmaMath<128, G> copies through 3-D maps
+      if (!encode_cache_map_halves(&maps.k, k_cache, d) || !encode_cache_map_halves(&maps.v, v_cache, d))
+        return PKV_ERR_CUDA;
+    } else if (pl.k.maps == MAPS_BF16) {
       if (!encode_cache_map(&maps.k, k_cache, d) || !encode_cache_map(&maps.v, v_cache, d)) return PKV_ERR_CUDA;
     } else if (!encode_fp8_maps(&maps, k_cache, v_cache, d)) {
       return PKV_ERR_CUDA;
