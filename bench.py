@@ -897,9 +897,12 @@ def fp8_step_entry(args, peak: float, local: int):
          "seq_steps_per_s": round(s.n / (t_step * 1e-3), 1),
          "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                       "frac": round(ach / peak, 4), "mean_launch_us": round(1e3 * dec_ms, 2),
-                      "kernel": "paged_decode_kernel<Fp8Math<4>,128,4>"},
+                      "kernel": "paged_decode_kernel<Fp8Math<4,3>,128,4,false>", "traffic": None},
          "timing": f"{args.steps} steps back to back (32 layers of cache write + decode each), inputs larger "
                    "than L2; roofline = decode launches of the next steps back to back"}
+    rec = decode_traffic_record("serve256_fp8")
+    if rec is not None:   # ncu DRAM bytes of one decode launch, scaled to this launch's bytes
+        e["roofline"]["traffic"] = int(rec["bytes_per_launch_profile"] * dec_bytes / rec["algorithmic_bytes_profile"])
     del s
     torch.cuda.empty_cache()
     return e
