@@ -1267,17 +1267,23 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   int32_t* cta_cnt = wsum + 16;
   if (threadIdx.x < NW) cta_cnt[threadIdx.x] = 0;
   set_error_word(a.err);
-  if (!a.late_wait) pdl_wait();
   // deferred mode: the CTA's first tasks, one per warp, taken at once, while the prefix is built
-  // (wsum[8] is not used by the prefix build)
-  if (kDefer && threadIdx.x == 0)
-    wsum[8] = static_cast<int32_t>(grab_tasks(a.ws_count, a.tag, static_cast<unsigned int>(NW), 0x7fffffff));
+  // (wsum[8] is not used by the prefix build); it uses the workspace, so it waits first
+  if constexpr (kDefer) {
+    if (!a.late_wait) pdl_wait();
+    if (threadIdx.x == 0)
+      wsum[8] = static_cast<int32_t>(grab_tasks(a.ws_count, a.tag, static_cast<unsigned int>(NW), 0x7fffffff));
+  }
   build_prefix(a, pref, ipref, cfirst, wsum);
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(smem_addr(bars + s), 1);
     fence_mbar_init();
   }
   __syncthreads();
+  // The prefix build above reads only context_lens (and may record a bad length); the caches, tables,
+  // q and workspace are read, and outputs written, only after this wait, so the build overlaps the
+  // tail of the kernel before (measured: serving step 4.297 -> 4.247 ms).
+  if (!kDefer && !a.late_wait) pdl_wait();
 
   const int W = gridDim.x * NW;
   const int w = blockIdx.x * NW + warp;
