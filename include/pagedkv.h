@@ -10,10 +10,10 @@
  * except pkv_last_error. Kernels are launched with programmatic dependent launch (unless
  * PKV_PDL=0): a decode kernel may start while the kernel before it on the stream is still
  * running, once that kernel allows it (griddepcontrol.launch_dependents; library kernels do so),
- * and reads context_lens before it waits for that kernel to finish; it reads the caches, tables,
- * q and the workspace, and writes its outputs, only after the wait (only a bad length may be
- * recorded in the error word before it). A kernel of the caller that allows its dependents to
- * launch early must not write context_lens after doing so.
+ * and reads context_lens and block_tables before it waits for that kernel to finish; it reads
+ * the caches, q and the workspace, and writes its outputs, only after the wait (only a bad length
+ * may be recorded in the error word before it). A kernel of the caller that allows its dependents
+ * to launch early must not write context_lens or block_tables after doing so.
  *
  * Method (sources are the pages this library implements):
  *  - KV state of a request lives in fixed-size physical blocks of B token positions

@@ -1280,23 +1280,21 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     fence_mbar_init();
   }
   __syncthreads();
-  // The prefix build above reads only context_lens (and may record a bad length); the caches, tables,
-  // q and workspace are read, and outputs written, only after this wait, so the build overlaps the
-  // tail of the kernel before (measured: serving step 4.297 -> 4.247 ms).
-  if (!kDefer && !a.late_wait) pdl_wait();
-
   const int W = gridDim.x * NW;
   const int w = blockIdx.x * NW + warp;
   const int64_t NP = static_cast<int64_t>(pref[n]) * Hkv;
 
-  // Empty sequences: zero rows (and a log-sum-exp of -inf: no weight in a later merge).
-  for (int32_t b = w; b < n; b += W) {
-    if (pref[b + 1] != pref[b]) continue;
-    float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(b) * a.Hq * D);
-    for (int i = lane; i < a.Hq * D / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.lse_out != nullptr)
-      for (int i = lane; i < a.Hq; i += 32) a.lse_out[static_cast<int64_t>(b) * a.Hq + i] = -INFINITY;
-  }
+  // Empty sequences: zero rows (and a log-sum-exp of -inf: no weight in a later merge). Outputs are
+  // written only after the dependency wait.
+  auto zero_empty = [&]() {
+    for (int32_t b = w; b < n; b += W) {
+      if (pref[b + 1] != pref[b]) continue;
+      float4* o = reinterpret_cast<float4*>(a.out + static_cast<int64_t>(b) * a.Hq * D);
+      for (int i = lane; i < a.Hq * D / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.lse_out != nullptr)
+        for (int i = lane; i < a.Hq; i += 32) a.lse_out[static_cast<int64_t>(b) * a.Hq + i] = -INFINITY;
+    }
+  };
 
   // Balanced mode splits the chunks over Weff = min(W, max(1, NP / mc)) warps, mc = min_chunks (half
   // of it below 8192 chunks in all): every range is non-empty (the merge relies on it) and problems
@@ -1315,6 +1313,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
   const int64_t Wmax = NP / mc > 0 ? NP / mc : 1;
   const int64_t Weff = Wmax < W ? Wmax : W;
   if constexpr (kDefer) {
+    zero_empty();
     const TaskMap tm = defer_task_map(NP, a.min_chunks, S, a.max_tasks);
     if (blockIdx.x == 0) {   // where the merging kernel finds each unit's parts
       for (int32_t i = threadIdx.x; i <= n; i += blockDim.x) {
@@ -1336,24 +1335,24 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
     pdl_launch_dependents();
     return;
   }
-  int64_t lo, hi;
+  int64_t lo = 0, hi = 0;
   if (PC == 0) {
-    if (w >= Weff) return;
-    lo = NP * w / Weff;
-    hi = NP * (w + 1) / Weff;
+    if (w < Weff) {
+      lo = NP * w / Weff;
+      hi = NP * (w + 1) / Weff;
+    }
   } else {
     const int64_t NI = static_cast<int64_t>(ipref[n]) * Hkv;
     lo = item_start(pref, ipref, n, Hkv, PC, NI * w / W);
     hi = item_start(pref, ipref, n, Hkv, PC, NI * (w + 1) / W);
   }
   const int64_t n_chunks = hi - lo;
-  if (n_chunks <= 0) return;
 
   // --- producer (lane 0 issues; the block-table window is spread over the lanes) ---
   // pf walks the chunks ahead of the consumer; (p_pg, p_sub) = its page in the block table and
   // chunk within that page, stepped without divisions except at unit changes.
   const int32_t cpb = a.B / kChunk;
-  Cursor pf = locate(pref, n, Hkv, lo);
+  Cursor pf = n_chunks > 0 ? locate(pref, n, Hkv, lo) : Cursor{0, 0, 0, 1};   // idle warps: unused
   int32_t p_pg = 0, p_sub = 0;
   auto p_unit_start = [&]() {
     const int32_t ch = (cfirst ? cfirst[pf.b] : 0) + pf.c;
@@ -1366,8 +1365,22 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
                                                     ((static_cast<int64_t>(pf.b) * a.Hq + pf.h * G) * D) * Math::kQElem +
                                                     128 * lane));
   };
-  p_unit_start();
   int32_t win_b = -1, win_base = 0, win_val = -1;
+  if (n_chunks > 0) {
+    p_unit_start();
+    // the first block-table window (an input, like context_lens)
+    win_b = pf.b;
+    win_base = p_pg;
+    const int32_t idx = win_base + lane;
+    win_val = idx < a.MB ? __ldg(a.block_tables + static_cast<int64_t>(pf.b) * a.MB + idx) : -1;
+  }
+  // The prefix build and the first block-table window above read only context_lens and block_tables;
+  // the caches, q and the workspace are read, and outputs written, only after this wait, so that work
+  // overlaps the tail of the kernel before (measured with the build alone: serving step 4.297 -> 4.247
+  // ms).
+  if (!a.late_wait) pdl_wait();
+  zero_empty();
+  if (n_chunks <= 0) return;
   const uint64_t policy = policy_evict_first();
   int64_t issued = 0;
 
@@ -1583,6 +1596,7 @@ __global__ void __launch_bounds__(128, Math::kMinCtasPerSm) paged_decode_kernel(
       mbar_wait_bounded(smem_addr(bars + static_cast<int>(k % S)), static_cast<uint32_t>((k / S) & 1));
   }
   if (pub) publish();
+  if (a.late_wait) pdl_wait();
   pdl_launch_dependents();
   if (pend) {
     if (pend_cta) {
